@@ -1,0 +1,81 @@
+"""Build ``libnvfp4.so`` in-tree with nvcc for sm_103a (GB300).
+
+Each ``csrc/*.cu`` translation unit is compiled in parallel, then linked into
+``nvfp4_block_scaled_act_gb300/libnvfp4.so`` with the CUDA runtime linked
+statically.  ``python -m nvfp4_block_scaled_act_gb300.build`` runs it.
+"""
+from __future__ import annotations
+
+import concurrent.futures
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+OBJ = os.path.join(PKG, "_build")
+LIB = os.path.join(PKG, "libnvfp4.so")
+SOURCES = ["api.cu", "quant.cu", "gemm_w4a4.cu", "gemv_w4a16.cu", "moe.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found")
+
+
+def _flags(verbose_ptxas: bool) -> list[str]:
+    f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
+                "--expt-relaxed-constexpr"]
+    if verbose_ptxas:
+        f += ["-Xptxas", "-v"]
+    return f
+
+
+def _newer(src_paths, out_path) -> bool:
+    if not os.path.exists(out_path):
+        return True
+    t = os.path.getmtime(out_path)
+    return any(os.path.getmtime(p) > t for p in src_paths)
+
+
+def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:
+    os.makedirs(OBJ, exist_ok=True)
+    headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))]
+    headers.append(os.path.join(INCLUDE, "nvfp4.h"))
+    cmds = []
+    objs = []
+    for s in SOURCES:
+        src = os.path.join(CSRC, s)
+        obj = os.path.join(OBJ, s.replace(".cu", ".o"))
+        objs.append(obj)
+        if force or verbose_ptxas or _newer([src] + headers, obj):
+            cmds.append([nvcc()] + _flags(verbose_ptxas) + ["-c", src, "-o", obj])
+    if cmds:
+        with concurrent.futures.ThreadPoolExecutor(max_workers=jobs or len(cmds)) as ex:
+            results = list(ex.map(lambda c: subprocess.run(c, capture_output=True, text=True), cmds))
+        failed = [r for r in results if r.returncode != 0]
+        for r in results:
+            if verbose_ptxas or r.returncode != 0:
+                sys.stderr.write(r.stdout + r.stderr)
+        if failed:
+            raise RuntimeError("nvcc failed")
+    if force or cmds or _newer(objs, LIB):
+        tmp = LIB + f".{os.getpid()}.tmp"
+        r = subprocess.run([nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs,
+                           capture_output=True, text=True)
+        if r.returncode != 0:
+            sys.stderr.write(r.stdout + r.stderr)
+            raise RuntimeError("link failed")
+        os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv)
+    print(LIB)

@@ -1,0 +1,433 @@
+// Block-scaled NVFP4 x NVFP4 GEMM on the sm_103a tensor cores
+// (tcgen05.mma kind::mxf4nvf4, scale_vec::4X: e2m1 operands, one UE4M3 scale per
+// 16 k-elements, fp32 accumulation in TMEM).
+//
+// Computes, for 128-row tiles of A and column tiles of B (both K-major NVFP4):
+//   acc[m, n] = sum_k e2m1(A[m,k]) s_A[m,k/16] * e2m1(B[n,k]) s_B[n,k/16]
+// and hands acc to one of four epilogues:
+//   kEpiDense      out = bf16(alpha * acc)                       (W4A4 linear)
+//   kEpiGatedQuant h = silu(alpha_e * G) * (alpha_e * U) -> NVFP4 codes/scales
+//                  (MoE gate_up: B tile = 128 gate rows then 128 up rows)
+//   kEpiGatedAmax  per-expert max |h| (calibration of the second input global)
+//   kEpiDownSum    y[t] += w_route * alpha_e * acc with fp32 vector reductions
+//                  (MoE down and top-k sum)
+// The W4A4 linear of "run nvfp4 linears on nvfp4 activations on sm_120" and the
+// warp-specialised gate_up / down GEMMs of the W4A4 MoE prefill page (both
+// section "Changes") were written for mma.sync on sm_120; this kernel keeps
+// their dataflow and epilogue fusion and maps it onto tcgen05 and TMEM.
+//
+// Structure (one CTA per SM, persistent over tiles n-fastest):
+//   warp 0      TMA producer: a 128x128-byte A box, BN/128 B boxes (128-byte
+//               swizzle) and the matching 512-byte scale atoms (bulk copies,
+//               contiguous in the 128x4 layout) into a STAGES-deep smem ring.
+//   warp 1      allocates TMEM; one lane copies each stage's scale atoms
+//               smem -> TMEM (tcgen05.cp 32x128b.warpx4) and issues 4 MMAs of
+//               K = 64 per 256-k stage; tcgen05.commit releases smem stages and
+//               publishes finished accumulators.
+//   warps 2..   epilogue: tcgen05.ld of the accumulator, fused epilogue math,
+//               global stores; an accumulator is released as soon as it has
+//               been read, so the next tile's MMAs overlap the epilogue math.
+// Every mbarrier wait is bounded; a timeout sets the device status word and
+// every role winds down (waiting for its own copies and MMAs) before TMEM is freed.
+#include "nvfp4_common.cuh"
+#include "nvfp4_internal.h"
+
+namespace nvfp4 {
+
+template <int BN_, int NUM_ACC_, int STAGES_, int NE_, int MODE_>
+struct GemmCfg {
+  static constexpr int BN = BN_;           // MMA N (B rows per tile)
+  static constexpr int NUM_ACC = NUM_ACC_;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int NE = NE_;           // epilogue warps (multiple of 4)
+  static constexpr int MODE = MODE_;
+  static constexpr int BM = 128;
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int NBLK = BN / 128;    // 128-row B boxes per stage
+  static constexpr int SFA_BYTES = 2048;   // 4 atoms = 256 k of 128 rows
+  static constexpr int SFB_BYTES = NBLK * 2048;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+  static constexpr int SF_COLS = 16 + 4 * (BN / 32);  // TMEM scale columns per stage
+  static constexpr int SF_BASE = NUM_ACC * BN;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int THREADS = 64 + 32 * NE;
+  static constexpr bool GROUPED = MODE != kEpiDense;
+  static_assert(SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+  static_assert(SMEM_BYTES <= 232448, "smem budget");
+  static_assert(NE % 4 == 0, "epilogue warps cover the four TMEM lane quadrants");
+};
+
+// ---------------------------------------------------------------------------
+// epilogue helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float silu_f32(float v) { return __fdiv_rn(v, __fadd_rn(1.0f, expf(-v))); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// Quantise 64 consecutive h values (four 16-blocks) of one row: 32 code bytes
+// and 4 scale bytes.
+__device__ __forceinline__ void quant64(const float (&h)[64], float g, uint4& c0, uint4& c1, uint32_t& s4) {
+  uint32_t words[8];
+  s4 = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    float v[16];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      v[i] = h[16 * b + i];
+      amax = fmaxf(amax, fabsf(v[i]));
+    }
+    const BlockScale bs = block_scale(amax, g);
+    const uint2 w = encode_block16(v, bs.r, bs.r == 0.0f);
+    words[2 * b] = w.x;
+    words[2 * b + 1] = w.y;
+    s4 |= bs.s8 << (8 * b);
+  }
+  c0 = make_uint4(words[0], words[1], words[2], words[3]);
+  c1 = make_uint4(words[4], words[5], words[6], words[7]);
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+    gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const GemmParams p) {
+  constexpr int STAGES = Cfg::STAGES;
+  constexpr int NUM_ACC = Cfg::NUM_ACC;
+  constexpr int BN = Cfg::BN;
+  constexpr int NE = Cfg::NE;
+  constexpr int MODE = Cfg::MODE;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t accf_bar[NUM_ACC];
+  __shared__ __align__(8) uint64_t acce_bar[NUM_ACC];
+  __shared__ __align__(8) uint64_t done_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < NUM_ACC; ++a) {
+      mbar_init(&accf_bar[a], 1);
+      mbar_init(&acce_bar[a], NE);
+    }
+    mbar_init(&done_bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_slot;
+
+  const int m_tiles = Cfg::GROUPED ? *p.d_m_tiles : p.m_tiles;
+  const int total = m_tiles * p.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t last_phase[STAGES];
+      bool issued[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) {
+        issued[s] = false;
+        last_phase[s] = 0;
+      }
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+        const int e = Cfg::GROUPED ? p.tile_expert[mt] : 0;
+        int b_row[Cfg::NBLK];
+        if (MODE == kEpiDense) {
+#pragma unroll
+          for (int j = 0; j < Cfg::NBLK; ++j) b_row[j] = nt * BN + 128 * j;
+        } else {
+          b_row[0] = e * p.b_rows_per_expert + nt * 128;
+          if (Cfg::NBLK > 1) b_row[Cfg::NBLK - 1] = b_row[0] + p.up_offset;
+        }
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, &abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const int ks = min(4, (p.K - kb * 256) / 64);
+          uint8_t* sA = smem + stage * Cfg::STAGE_BYTES;
+          uint8_t* sB = sA + Cfg::A_BYTES;
+          uint8_t* sSFA = sB + Cfg::B_BYTES;
+          uint8_t* sSFB = sSFA + Cfg::SFA_BYTES;
+          uint32_t bytes = Cfg::A_BYTES + ks * 512;
+#pragma unroll
+          for (int j = 0; j < Cfg::NBLK; ++j)
+            if (b_row[j] < p.b_rows_total) bytes += 128 * 128 + ks * 512;
+          mbar_arrive_expect_tx(&full_bar[stage], bytes);
+          tma_load_2d(sA, &tmA, &full_bar[stage], kb * 128, mt * 128);
+          bulk_load(sSFA, p.sfa + (static_cast<int64_t>(mt) * p.sf_atoms + kb * 4) * 512, ks * 512,
+                    &full_bar[stage]);
+#pragma unroll
+          for (int j = 0; j < Cfg::NBLK; ++j) {
+            if (b_row[j] < p.b_rows_total) {
+              tma_load_2d(sB + j * 128 * 128, &tmB, &full_bar[stage], kb * 128, b_row[j]);
+              bulk_load(sSFB + j * 2048, p.sfb + (static_cast<int64_t>(b_row[j] >> 7) * p.sf_atoms + kb * 4) * 512,
+                        ks * 512, &full_bar[stage]);
+            }
+          }
+          issued[stage] = true;
+          last_phase[stage] = phase;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // every copy this thread started lands before the CTA can exit
+      int drain_abort = 0;
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s)
+        if (issued[s]) mbar_wait(&full_bar[s], last_phase[s], reinterpret_cast<volatile int*>(&drain_abort), p.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_nvfp4(128, BN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1, &abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, &abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int ks = min(4, (p.K - kb * 256) / 64);
+          const uint32_t sA = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+          const uint32_t sB = sA + Cfg::A_BYTES;
+          const uint32_t sSFA = sB + Cfg::B_BYTES;
+          const uint32_t sSFB = sSFA + Cfg::SFA_BYTES;
+          const uint32_t t_sfa = tmem_base + Cfg::SF_BASE + stage * Cfg::SF_COLS;
+          const uint32_t t_sfb = t_sfa + 16;
+          for (int s = 0; s < ks; ++s) {
+            tmem_cp_32x128b_x4(t_sfa + 4 * s, desc_scale_atom(sSFA + 512 * s));
+#pragma unroll
+            for (int j = 0; j < Cfg::NBLK; ++j)
+              tmem_cp_32x128b_x4(t_sfb + (BN / 32) * s + 4 * j, desc_scale_atom(sSFB + j * 2048 + 512 * s));
+          }
+          for (int s = 0; s < ks; ++s) {
+            umma_nvfp4(d_tmem, desc_kmajor_sw128(sA + 32 * s), desc_kmajor_sw128(sB + 32 * s), idesc,
+                       t_sfa + 4 * s, t_sfb + (BN / 32) * s, (kb > 0 || s > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&accf_bar[acc]);
+        if (++acc == NUM_ACC) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // wait until every MMA and copy issued above has completed
+      umma_commit(&done_bar);
+      int drain_abort = 0;
+      mbar_wait(&done_bar, 0, reinterpret_cast<volatile int*>(&drain_abort), p.status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int q = warp & 3;          // TMEM lane quadrant of this warp
+    const int part = ew >> 2;        // column part of this warp within its quadrant
+    constexpr int PARTS = NE / 4;
+    uint32_t acc = 0, acc_phase = 0;
+    const float alpha_dense = (MODE == kEpiDense) ? __ldg(p.alpha) : 0.0f;
+    const float g_out = (MODE == kEpiGatedQuant) ? __ldg(p.g_out) : 0.0f;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+      if (!mbar_wait(&accf_bar[acc], acc_phase, &abort_flag, p.status)) break;
+      tc_fence_after();
+      const int row = 32 * q + lane;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
+
+      if constexpr (MODE == kEpiDense) {
+        constexpr int COLS = BN / PARTS;
+        const int m = mt * 128 + row;
+        for (int c0 = part * COLS; c0 < (part + 1) * COLS; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + c0, r);
+          tmem_ld_wait();
+          const int n0 = nt * BN + c0;
+          if (m < p.M) {
+            uint16_t* dst = p.out + static_cast<int64_t>(m) * p.ldo + n0;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (n0 + 8 * v < p.N) {
+                uint4 o;
+                o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * alpha_dense, __uint_as_float(r[8 * v + 1]) * alpha_dense);
+                o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * alpha_dense, __uint_as_float(r[8 * v + 3]) * alpha_dense);
+                o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * alpha_dense, __uint_as_float(r[8 * v + 5]) * alpha_dense);
+                o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * alpha_dense, __uint_as_float(r[8 * v + 7]) * alpha_dense);
+                *reinterpret_cast<uint4*>(dst + 8 * v) = o;
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce_bar[acc]);
+      } else if constexpr (MODE == kEpiGatedQuant || MODE == kEpiGatedAmax) {
+        // accumulator columns [0, 128) = gate, [128, 256) = up; this warp owns
+        // h columns [64 * part, 64 * part + 64)
+        uint32_t g0[32], g1[32], u0[32], u1[32];
+        tmem_ld_32x32b_x32(t_row + 64 * part, g0);
+        tmem_ld_32x32b_x32(t_row + 64 * part + 32, g1);
+        tmem_ld_32x32b_x32(t_row + 128 + 64 * part, u0);
+        tmem_ld_32x32b_x32(t_row + 128 + 64 * part + 32, u1);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce_bar[acc]);
+        const int prow = mt * 128 + row;
+        const int rm = p.row_map[prow];
+        const int e = p.tile_expert[mt];
+        const float a = __ldg(p.alpha + e);
+        float h[64];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          h[i] = __fmul_rn(silu_f32(__fmul_rn(a, __uint_as_float(g0[i]))), __fmul_rn(a, __uint_as_float(u0[i])));
+          h[32 + i] =
+              __fmul_rn(silu_f32(__fmul_rn(a, __uint_as_float(g1[i]))), __fmul_rn(a, __uint_as_float(u1[i])));
+        }
+        if constexpr (MODE == kEpiGatedQuant) {
+          if (rm >= 0) {
+            uint4 c0, c1;
+            uint32_t s4;
+            quant64(h, g_out, c0, c1, s4);
+            uint8_t* dst = p.q_codes + static_cast<int64_t>(prow) * p.q_row_bytes + nt * 64 + part * 32;
+            reinterpret_cast<uint4*>(dst)[0] = c0;
+            reinterpret_cast<uint4*>(dst)[1] = c1;
+            const int64_t c = static_cast<int64_t>(nt) * 8 + part * 4;
+            *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(prow, c, p.q_cpad4)) = s4;
+          }
+        } else {
+          float m = 0.0f;
+          if (rm >= 0) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(h[i]));
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+          if (lane == 0 && m > 0.0f) atomicMax(p.amax + e, __float_as_uint(m));
+        }
+      } else {
+        // routed down projection: y[t, n] += w_route * alpha_e * acc
+        const int prow = mt * 128 + row;
+        const int rm = p.row_map[prow];
+        const int e = p.tile_expert[mt];
+        float scale = 0.0f;
+        float* dst = nullptr;
+        if (rm >= 0) {
+          scale = __fmul_rn(__ldg(p.topk_w + rm), __ldg(p.alpha + e));
+          dst = p.y + static_cast<int64_t>(rm / p.topk) * p.ldy + nt * BN;
+        }
+        constexpr int COLS = BN / PARTS;
+        for (int c0 = part * COLS; c0 < (part + 1) * COLS; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + c0, r);
+          tmem_ld_wait();
+          if (rm >= 0) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              red_add_v4(dst + c0 + 4 * v, __uint_as_float(r[4 * v]) * scale, __uint_as_float(r[4 * v + 1]) * scale,
+                         __uint_as_float(r[4 * v + 2]) * scale, __uint_as_float(r[4 * v + 3]) * scale);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce_bar[acc]);
+      }
+      if (++acc == NUM_ACC) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+using DenseCfg = GemmCfg<128, 2, 6, 4, kEpiDense>;
+using GatedCfg = GemmCfg<256, 1, 4, 8, kEpiGatedQuant>;
+using AmaxCfg = GemmCfg<256, 1, 4, 8, kEpiGatedAmax>;
+using DownCfg = GemmCfg<128, 2, 6, 4, kEpiDownSum>;
+
+template <class Cfg>
+static cudaError_t launch_cfg(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_nvfp4_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  gemm_nvfp4_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(maps.a, maps.b, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {
+  switch (mode) {
+    case kEpiDense: return launch_cfg<DenseCfg>(maps, p, grid, stream);
+    case kEpiGatedQuant: return launch_cfg<GatedCfg>(maps, p, grid, stream);
+    case kEpiGatedAmax: return launch_cfg<AmaxCfg>(maps, p, grid, stream);
+    case kEpiDownSum: return launch_cfg<DownCfg>(maps, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int gemm_max_ctas_per_sm(int) { return 1; }
+
+}  // namespace nvfp4

@@ -1,0 +1,277 @@
+// MoE routing kernels around the grouped GEMMs (layer flow "align -> gate_up ->
+// act -> down -> sum" of "speed up the nvfp4 moe prefill gemm on rtx gpus",
+// section "Changes"; static input scales and top-k sum of the W4A4 MoE prefill
+// page, section "Changes").
+//
+// align: a stable counting sort of the T * topk routes by expert, each
+// expert's segment padded to a multiple of 128 rows (one GEMM tile):
+//   moe_hist_kernel     per 1024-route chunk, routes per expert
+//   moe_scan_kernel     one block: expert offsets, padded tile table,
+//                       per-chunk bases, padding rows of row_map
+//   moe_scatter_kernel  per chunk, in route order: row_map / pos entries
+// The order inside a segment is the route order, so the layout is the same on
+// every run.  Nothing leaves the device: the tile count is read by the GEMMs.
+//
+// quant_permute: the NVFP4 quantisation of x with the static global g_a1, one
+// warp per 256-element chunk of a token row, written to each of the token's
+// permuted rows; it also clears the fp32 top-k accumulator y.
+// finalize: y (fp32) -> bf16.
+#include "nvfp4_common.cuh"
+#include "nvfp4_internal.h"
+#include "nvfp4_moe.h"
+
+namespace nvfp4 {
+
+constexpr int kChunk = 1024;  // routes per histogram / scatter block
+
+__global__ void __launch_bounds__(256) moe_hist_kernel(const int32_t* __restrict__ ids, int64_t R, int E,
+                                                       int32_t* __restrict__ hist, int* status) {
+  extern __shared__ int32_t sh[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+  __syncthreads();
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunk;
+  for (int i = threadIdx.x; i < kChunk; i += blockDim.x) {
+    const int64_t r = base + i;
+    if (r < R) {
+      const int e = ids[r];
+      if (e >= 0 && e < E)
+        atomicAdd(&sh[e], 1);
+      else
+        record_status(status, kStatusBadExpert);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<int64_t>(blockIdx.x) * E + e] = sh[e];
+}
+
+// One block of up to 1024 threads, one expert per thread.
+__global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
+                                                        int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                        int32_t* __restrict__ n_tiles, int32_t* __restrict__ row_map,
+                                                        int32_t* __restrict__ tile_expert) {
+  __shared__ int32_t warp_sums[32];
+  const int e = threadIdx.x;
+  int32_t cnt = 0;
+  if (e < E)
+    for (int c = 0; c < nchunks; ++c) cnt += hist[static_cast<int64_t>(c) * E + e];
+  const int32_t padded = (cnt + 127) / 128 * 128;
+  // exclusive scan of padded over experts (block-wide)
+  int32_t v = padded;
+  const int lane = e & 31, w = e >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += t;
+  }
+  if (lane == 31) warp_sums[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int32_t s = (lane < static_cast<int>(blockDim.x >> 5)) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t t = __shfl_up_sync(0xFFFFFFFFu, s, o);
+      if (lane >= o) s += t;
+    }
+    warp_sums[lane] = s;
+  }
+  __syncthreads();
+  const int32_t incl = v + (w > 0 ? warp_sums[w - 1] : 0);
+  const int32_t off = incl - padded;
+  if (e < E) {
+    counts[e] = cnt;
+    offsets[e] = off;
+    // per-chunk bases, in chunk order
+    int32_t run = off;
+    for (int c = 0; c < nchunks; ++c) {
+      const int64_t idx = static_cast<int64_t>(c) * E + e;
+      const int32_t h = hist[idx];
+      hist[idx] = run;
+      run += h;
+    }
+    for (int32_t p = off + cnt; p < off + padded; ++p) row_map[p] = -1;
+    for (int32_t p = off; p < off + padded; p += 128) tile_expert[p / 128] = e;
+  }
+  if (e == E - 1) {
+    offsets[E] = incl;
+    *n_tiles = incl / 128;
+  }
+}
+
+// One warp per chunk; routes in order, 32 at a time.
+__global__ void __launch_bounds__(32) moe_scatter_kernel(const int32_t* __restrict__ ids, int64_t R, int E,
+                                                         const int32_t* __restrict__ hist,
+                                                         int32_t* __restrict__ row_map, int32_t* __restrict__ pos) {
+  extern __shared__ int32_t run[];
+  for (int e = threadIdx.x; e < E; e += 32) run[e] = hist[static_cast<int64_t>(blockIdx.x) * E + e];
+  __syncwarp();
+  const int lane = threadIdx.x;
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunk;
+  for (int i0 = 0; i0 < kChunk; i0 += 32) {
+    const int64_t r = base + i0 + lane;
+    const bool in = r < R;
+    const int e = in ? ids[r] : -1;
+    const bool valid = in && e >= 0 && e < E;
+    const unsigned key = valid ? static_cast<unsigned>(e) : 0xFFFFFFFFu;
+    const unsigned same = __match_any_sync(0xFFFFFFFFu, key);
+    const int rank = __popc(same & ((1u << lane) - 1u));
+    int32_t p = -1;
+    if (valid) {
+      p = run[e] + rank;
+      row_map[p] = static_cast<int32_t>(r);
+    }
+    if (in) pos[r] = p;
+    __syncwarp();
+    if (valid && rank == 0) run[e] += __popc(same);
+    __syncwarp();
+  }
+}
+
+// x [T, H] bf16 -> NVFP4 rows of a1 at pos[t * topk + s]; clears y [T, H].
+__global__ void __launch_bounds__(256) moe_quant_permute_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H,
+                                                                int topk, const float* __restrict__ d_g,
+                                                                const int32_t* __restrict__ pos,
+                                                                uint8_t* __restrict__ a_codes,
+                                                                uint8_t* __restrict__ a_sf, int64_t cpad4,
+                                                                float* __restrict__ y) {
+  const float g = __ldg(d_g);
+  const int lane = threadIdx.x & 31;
+  const int64_t chunks = (H + 255) / 256;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; item < T * chunks;
+       item += nwarps) {
+    const int64_t t = item / chunks;
+    const int64_t ch = item - t * chunks;
+    const int64_t k0 = ch * 256 + lane * 8;
+    const bool real = k0 < H;
+    float v[8];
+    float amax = 0.0f;
+    if (real) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(x + t * H + k0));
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] = bf16_bits_to_f32(w[j] & 0xFFFFu);
+        v[2 * j + 1] = bf16_bits_to_f32(w[j] >> 16);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+      float4* yz = reinterpret_cast<float4*>(y + t * H + k0);
+      yz[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      yz[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    const BlockScale bs = block_scale(amax, g);
+    uint32_t packed = 0;
+    if (bs.r != 0.0f) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        packed |= f32x2_to_e2m1x2(__fmul_rn(v[2 * j], bs.r), __fmul_rn(v[2 * j + 1], bs.r)) << (8 * j);
+    }
+    if (real) {
+      const int64_t c = k0 / 16;
+      for (int s = 0; s < topk; ++s) {
+        const int32_t p = pos[t * topk + s];
+        if (p < 0) continue;
+        *reinterpret_cast<uint32_t*>(a_codes + static_cast<int64_t>(p) * (H / 2) + k0 / 2) = packed;
+        if ((lane & 1) == 0) a_sf[sf_offset(p, c, cpad4)] = static_cast<uint8_t>(bs.s8);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) moe_finalize_kernel(const float* __restrict__ y, int64_t n,
+                                                           uint16_t* __restrict__ out) {
+  for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x * 8) {
+    const float4 a = reinterpret_cast<const float4*>(y + i)[0];
+    const float4 b = reinterpret_cast<const float4*>(y + i)[1];
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y), h1 = __floats2bfloat162_rn(a.z, a.w);
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y), h3 = __floats2bfloat162_rn(b.z, b.w);
+    uint4 o;
+    o.x = *reinterpret_cast<uint32_t*>(&h0);
+    o.y = *reinterpret_cast<uint32_t*>(&h1);
+    o.z = *reinterpret_cast<uint32_t*>(&h2);
+    o.w = *reinterpret_cast<uint32_t*>(&h3);
+    *reinterpret_cast<uint4*>(out + i) = o;
+  }
+}
+
+// Dense calibration routing: route (t, e) for every row t and expert e.
+__global__ void moe_dense_ids_kernel(int32_t* __restrict__ ids, int64_t Tc, int E) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < Tc * E;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    ids[i] = static_cast<int32_t>(i % E);
+}
+
+// amax bits [E] -> g_e = 2688 / amax_e (1 when zero); *g_max = max_e g_e; the
+// amax values are rewritten as floats for the caller.
+__global__ void __launch_bounds__(1024) moe_calib_finish_kernel(unsigned int* __restrict__ amax_bits, int E,
+                                                                float* __restrict__ g_max) {
+  __shared__ float wm[32];
+  float g = -INFINITY;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const float a = __uint_as_float(amax_bits[e]);
+    g = fmaxf(g, a > 0.0f ? __fdiv_rn(2688.0f, a) : 1.0f);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) g = fmaxf(g, __shfl_xor_sync(0xFFFFFFFFu, g, o));
+  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = g;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = -INFINITY;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) m = fmaxf(m, wm[i]);
+    *g_max = m;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_moe_align(const int32_t* ids, int64_t T, int topk, int E, const MoEWorkspace& w, int* status,
+                             cudaStream_t stream) {
+  const int64_t R = T * topk;
+  const int nchunks = static_cast<int>((R + kChunk - 1) / kChunk);
+  moe_hist_kernel<<<nchunks, 256, E * sizeof(int32_t), stream>>>(ids, R, E, w.hist, status);
+  moe_scan_kernel<<<1, 1024, 0, stream>>>(w.hist, nchunks, E, w.counts, w.offsets, w.n_tiles, w.row_map,
+                                          w.tile_expert);
+  moe_scatter_kernel<<<nchunks, 32, E * sizeof(int32_t), stream>>>(ids, R, E, w.hist, w.row_map, w.pos);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_quant_permute(const void* x, int64_t T, int64_t H, int topk, const float* d_g,
+                                     const MoEWorkspace& w, int num_sms, cudaStream_t stream) {
+  const int64_t items = T * ((H + 255) / 256);
+  int64_t blocks = (items + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  moe_quant_permute_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(x), T, H, topk, d_g, w.pos, w.a1_codes, w.a1_sf, (H / 16 + 3) / 4, w.y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_finalize(const float* y, int64_t n, void* out, int num_sms, cudaStream_t stream) {
+  int64_t blocks = (n / 8 + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  moe_finalize_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(y, n, static_cast<uint16_t*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_dense_ids(int32_t* ids, int64_t Tc, int E, cudaStream_t stream) {
+  const int64_t n = Tc * E;
+  const int blocks = static_cast<int>((n + 255) / 256 > 4096 ? 4096 : (n + 255) / 256);
+  moe_dense_ids_kernel<<<blocks < 1 ? 1 : blocks, 256, 0, stream>>>(ids, Tc, E);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_calib_finish(unsigned int* amax_bits, int E, float* g_max, cudaStream_t stream) {
+  moe_calib_finish_kernel<<<1, 1024, 0, stream>>>(amax_bits, E, g_max);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,70 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+// Every launcher enqueues on `stream` and returns cudaGetLastError().
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+// ---- quantisation (quant.cu) ----------------------------------------------
+cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, const float* d_global,
+                             uint8_t* codes, uint8_t* scales, cudaStream_t stream);
+cudaError_t launch_compute_global(const void* x, int64_t rows, int64_t cols, int64_t ldx, float* d_global,
+                                  cudaStream_t stream, int num_sms);
+cudaError_t launch_make_alpha(const float* d_g_a, const float* d_g_w, int64_t n, float* d_alpha,
+                              cudaStream_t stream);
+cudaError_t launch_reduce_max(const float* d_in, int64_t n, float* d_out, cudaStream_t stream);
+
+// ---- block-scaled tcgen05 GEMM (gemm_w4a4.cu) ------------------------------
+enum EpiMode : int { kEpiDense = 0, kEpiGatedQuant = 1, kEpiGatedAmax = 2, kEpiDownSum = 3 };
+
+struct GemmParams {
+  const uint8_t* sfa;      // swizzled scales of A (over all A rows)
+  const uint8_t* sfb;      // swizzled scales of B (over all B rows)
+  int K;                   // reduction length (multiple of 64)
+  int kblocks;             // ceil(K / 256)
+  int sf_atoms;            // K / 64: 512-byte scale atoms per 128-row block
+  int n_tiles;             // output column tiles
+  int m_tiles;             // dense: ceil(M / 128)
+  const int* d_m_tiles;    // grouped: device count of 128-row tiles
+  const int* tile_expert;  // grouped: expert of each 128-row tile
+  const int* row_map;      // grouped: route id of each permuted row, -1 = padding
+  int b_rows_per_expert;   // grouped: B rows per expert (2I or H)
+  int up_offset;           // gated: row offset of the up half (I)
+  int b_rows_total;        // rows of B
+  const float* alpha;      // dense: [1]; grouped: [E]
+  // dense output
+  uint16_t* out;
+  int64_t ldo;
+  int M;
+  int N;
+  // gated output (NVFP4 of SiLU(gate) * up)
+  const float* g_out;
+  uint8_t* q_codes;
+  uint8_t* q_sf;
+  int64_t q_row_bytes;     // I / 2
+  int64_t q_cpad4;         // padded scale columns / 4 of the intermediate
+  unsigned int* amax;      // calibration: per-expert amax bits
+  // routed down output
+  float* y;
+  int64_t ldy;
+  const float* topk_w;
+  int topk;
+  int* status;
+};
+
+struct GemmMaps {
+  CUtensorMap a;
+  CUtensorMap b;
+};
+
+// Build a 2D TMA map over a [rows, row_bytes] byte matrix, box 128 x 128 bytes,
+// 128-byte swizzle.
+bool make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes);
+
+cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream);
+int gemm_max_ctas_per_sm(int mode);
+
+}  // namespace nvfp4

@@ -1,0 +1,57 @@
+// MoE workspace carving and launchers (moe.cu), shared with api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+struct MoEWorkspace {
+  int32_t* counts;       // [E]
+  int32_t* offsets;      // [E + 1]
+  int32_t* n_tiles;      // [1]
+  int32_t* row_map;      // [P_max]
+  int32_t* tile_expert;  // [P_max / 128]
+  int32_t* pos;          // [T * topk]
+  int32_t* hist;         // [nchunks * E]
+  int32_t* ids;          // [T * topk] (calibration routes)
+  uint8_t* a1_codes;     // [P_max, H/2]
+  uint8_t* a1_sf;        // swizzled over P_max rows, H/16 columns
+  uint8_t* h_codes;      // [P_max, I/2]
+  uint8_t* h_sf;         // swizzled over P_max rows, I/16 columns
+  float* y;              // [T, H]
+  unsigned int* amax;    // [E] (calibration)
+  int64_t p_max;
+};
+
+struct MoELayoutBytes {
+  size_t counts, offsets, n_tiles, row_map, tile_expert, pos, hist, ids, a1_codes, a1_sf, h_codes, h_sf, y, amax,
+      total;
+  int64_t p_max;
+};
+
+MoELayoutBytes moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk);
+MoEWorkspace moe_carve(void* base, const MoELayoutBytes& L);
+
+cudaError_t launch_moe_align(const int32_t* ids, int64_t T, int topk, int E, const MoEWorkspace& w, int* status,
+                             cudaStream_t stream);
+cudaError_t launch_moe_quant_permute(const void* x, int64_t T, int64_t H, int topk, const float* d_g,
+                                     const MoEWorkspace& w, int num_sms, cudaStream_t stream);
+cudaError_t launch_moe_finalize(const float* y, int64_t n, void* out, int num_sms, cudaStream_t stream);
+cudaError_t launch_moe_dense_ids(int32_t* ids, int64_t Tc, int E, cudaStream_t stream);
+cudaError_t launch_moe_calib_finish(unsigned int* amax_bits, int E, float* g_max, cudaStream_t stream);
+
+// ---- W4A16 decode (gemv_w4a16.cu) -------------------------------------------
+struct GemvPlan {
+  int splits;      // k-splits (1 = no workspace)
+  int kc;          // k elements per split (multiple of 128)
+  int row_blocks;  // ceil(N / 128)
+  size_t ws_bytes;
+};
+GemvPlan gemv_plan(int64_t T, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_gemv_w4a16(const void* x, int64_t T, int64_t ldx, const uint8_t* w_codes, const uint8_t* w_sf,
+                              int64_t N, int64_t K, const float* d_alpha, void* out, int64_t ldo, float* ws,
+                              const GemvPlan& plan, cudaStream_t stream);
+
+}  // namespace nvfp4

@@ -1,0 +1,108 @@
+"""The C-ABI library loads on a machine without a GPU, exports every function
+include/nvfp4.h declares, and refuses bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_block_scaled_act_gb300 as nv
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nvfp4_block_scaled_act_gb300 import build
+    build.build()
+    return nv.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 14
+    raw = ctypes.CDLL(nv.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), f"{n} declared in nvfp4.h but not exported"
+        assert n in nv.SIGNATURES, f"{n} has no Python binding"
+
+
+def test_status_strings(lib):
+    for s in range(9):
+        assert lib.nvfp4_status_string(s)
+    assert lib.nvfp4_version() >= 100
+
+
+@pytest.mark.parametrize("rows,k", [(1, 16), (8, 512), (130, 64), (7168, 5120), (300, 112)])
+def test_scale_bytes_matches_oracle(lib, rows, k):
+    assert lib.nvfp4_scale_bytes(rows, k) == oracle.scale_bytes(rows, k)
+
+
+P = ctypes.c_void_p(256)  # an aligned, never dereferenced address
+
+
+def test_w4a4_argument_errors(lib):
+    f = lib.nvfp4_linear_w4a4
+    assert f(P, P, 8, P, P, 12, 512, P, P, 12, None) == 2        # N % 8 (N = 12 refused)
+    assert f(P, P, 8, P, P, 16, 96, P, P, 16, None) == 2         # K % 64
+    assert f(P, P, 8, P, P, 16, 512, P, P, 8, None) == 1         # ldo < N
+    assert f(P, P, -1, P, P, 16, 512, P, P, 16, None) == 1       # negative M
+    assert f(P, P, 0, P, P, 16, 512, P, P, 16, None) == 0        # M = 0: nothing to do
+    assert f(ctypes.c_void_p(257), P, 8, P, P, 16, 512, P, P, 16, None) == 3
+    assert f(None, P, 8, P, P, 16, 512, P, P, 16, None) == 1
+
+
+def test_quant_and_w4a16_argument_errors(lib):
+    q = lib.nvfp4_quantize_act
+    assert q(P, 4, 24, 24, P, P, P, None) == 2                    # K % 16
+    assert q(P, 4, 32, 16, P, P, P, None) == 1                    # ldx < K
+    assert q(P, 4, 32, 36, P, P, P, None) == 3                    # ldx % 8
+    assert q(P, 0, 32, 32, P, P, P, None) == 0
+    g = lib.nvfp4_linear_w4a16
+    assert g(P, 17, 512, P, P, 64, 512, P, P, 64, None, 0, None) == 2   # T > 16
+    assert g(P, 4, 512, P, P, 64, 192, P, P, 64, None, 0, None) == 2    # K % 128
+    assert g(P, 0, 512, P, P, 64, 512, P, P, 64, None, 0, None) == 0
+
+
+def test_no_device_is_reported_without_a_gpu(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.nvfp4_linear_w4a4(P, P, 8, P, P, 16, 512, P, P, 16, None) == 8
+
+
+def test_moe_workspace_layout(lib):
+    T, H, I, E, topk = 4096, 2048, 768, 128, 8
+    lay = nv.nvfp4_moe_workspace_layout(T, H, I, E, topk)
+    assert lay.p_max == (T * topk + E * 127 + 127) // 128 * 128
+    assert lay.total == lib.nvfp4_moe_workspace(T, H, I, E, topk)
+    offs = [lay.counts, lay.offsets, lay.n_tiles, lay.row_map, lay.tile_expert, lay.pos, lay.a1_codes,
+            lay.a1_sf, lay.h_codes, lay.h_sf, lay.y, lay.hist]
+    assert all(o % 256 == 0 for o in offs)
+    assert lay.y + 4 * T * H <= lay.total
+    assert lay.h_codes + lay.p_max * I // 2 <= lay.h_sf
+    f = lib.nvfp4_moe_w4a4
+    args = [P, 16, 2048, 768, 128, 33] + [P] * 12 + [ctypes.c_size_t(1 << 40), None]
+    assert f(*args) == 2   # topk > 32
+    args[5] = 8
+    args[2] = 2000
+    assert f(*args) == 2   # H % 128
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        nv.load_library.__wrapped__ if hasattr(nv.load_library, "__wrapped__") else None
+        saved = nv._lib
+        nv._lib = None
+        try:
+            nv.load_library(str(tmp_path / "libnvfp4.so"))
+        finally:
+            nv._lib = saved
