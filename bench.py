@@ -1,0 +1,459 @@
+"""Benchmark of the NVFP4 hot path on GB300.
+
+One step runs every stage of the path once on synthetic inputs shaped like
+the pages' workloads, inputs resident in HBM:
+  prefill  activation quantisation + W4A4 block-scaled GEMM of the fused
+           qkv-style linear (M = 8192 tokens, N = 5120 + 1024 + 1024, K = 5120)
+  decode   W4A16 GEMM at T = 1, 2, 4, 8, 16 on (N, K) = (8704, 5120) and
+           (5120, 4352), each a CUDA graph over >= 2.5 GB of distinct weight
+           copies so that every call reads its weight from HBM
+  moe      the W4A4 MoE layer, E = 128, top-8, hidden 2048, intermediate 768,
+           T = 4096 (align, permute+quantise, gate_up with SiLU*up and NVFP4
+           requantisation, down with routing weight and top-k sum, bf16)
+The L2 is flushed (a 256 MiB write) before each stage; the flush is outside
+the timed events.  `value` is the W4A4 prefill throughput in TFLOP/s (the
+first clause of the metric); the decode GB/s and MoE TFLOP/s are reported in
+their own objects.  Multi-GPU: replicas (each rank runs the same step on its
+own GPU, weak scaling).
+
+--impl reference times the CPU oracle (the only reference this path has) on
+a bounded sample of the same prefill workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synthdata  # noqa: E402
+
+METRIC = "W4A4 prefill TFLOP/s (frac of FP4 peak); W4A16 decode HBM GB/s at T=1..16"
+PREFILL_M = 8192
+MOE_T = 4096
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio of GB300
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        try:
+            lines = [ln.split(",") for ln in open(self.path).read().strip().splitlines() if ln.strip()]
+        except Exception:
+            return out
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for f in lines:
+            f = [x.strip() for x in f]
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if sm:
+            out.update(sm_mhz=statistics.median(sm), sm_max_mhz=max(mx), reasons=sorted(reasons), samples=len(sm))
+        return out
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+
+class Workload:
+    def __init__(self, dev, nv):
+        self.nv = nv
+        self.dev = dev
+        self.lib = nv.load_library()
+        # prefill (fused qkv linear)
+        pc = synthdata.prefill_case(PREFILL_M, seed=0, device=dev)
+        self.pre_W = nv.quantize_weight(pc.w_parts)
+        self.pre_x = pc.x
+        self.pre_g = nv.nvfp4_compute_global(pc.x_calib)
+        self.pre_alpha = nv.nvfp4_make_alpha(self.pre_g, self.pre_W.g)
+        self.pre_codes, self.pre_sf = nv.nvfp4_quantize_act(self.pre_x, self.pre_g)
+        self.pre_out = torch.empty(PREFILL_M, self.pre_W.N, dtype=torch.bfloat16, device=dev)
+        self.pre_flops = 2.0 * PREFILL_M * self.pre_W.N * self.pre_W.K
+        N, K, M = self.pre_W.N, self.pre_W.K, PREFILL_M
+        self.pre_bytes = N * K // 2 + nv.nvfp4_scale_bytes(N, K) + M * K // 2 + nv.nvfp4_scale_bytes(M, K) + 2 * M * N
+        self.quant_bytes = M * K * 2 + M * K // 2 + nv.nvfp4_scale_bytes(M, K)
+        # decode
+        self.decode = []
+        for (N, K) in synthdata.DECODE_SHAPES:
+            d = synthdata.decode_case(16, N, K, seed=1, device=dev)
+            W = nv.quantize_weight(d.w_parts)
+            alpha = nv.nvfp4_make_alpha(None, W.g)
+            wbytes = N * K // 2 + nv.nvfp4_scale_bytes(N, K)
+            ncopy = max(2, int(2.5e9 // wbytes) + 1)
+            codes = [W.codes] + [W.codes.clone() for _ in range(ncopy - 1)]
+            scales = [W.scales] + [W.scales.clone() for _ in range(ncopy - 1)]
+            for T in synthdata.DECODE_TOKENS:
+                x = d.x[:T].contiguous()
+                out = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
+                wsb = nv.nvfp4_linear_w4a16_workspace(T, N, K)
+                ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+                self.decode.append(dict(N=N, K=K, T=T, x=x, out=out, ws=ws, wsb=wsb, codes=codes, scales=scales,
+                                        alpha=alpha, ncopy=ncopy, wbytes=wbytes,
+                                        bytes=wbytes + 2 * T * K + 2 * T * N, graph=None,
+                                        launches=1 + (1 if wsb > 0 else 0)))
+        # MoE
+        cfg = synthdata.MOE_SMALL
+        E, H, I, topk = cfg["E"], cfg["H"], cfg["I"], cfg["topk"]
+        mc = synthdata.moe_case(MOE_T, E, H, I, topk, cfg["skewed"], seed=0, device=dev)
+        self.moe_W = nv.quantize_moe_weights(lambda e: mc.w13(e), lambda e: mc.w2(e), E, H, I, dev)
+        self.moe_g_a1 = nv.nvfp4_compute_global(mc.x_calib)
+        self.moe_a13 = nv.nvfp4_make_alpha(self.moe_g_a1, self.moe_W.g13)
+        self.moe_g_a2, _ = nv.nvfp4_moe_calibrate(mc.x_calib, self.moe_g_a1, self.moe_W.w13_codes,
+                                                  self.moe_W.w13_sf, self.moe_a13, E, I)
+        self.moe_a2 = nv.nvfp4_make_alpha(self.moe_g_a2, self.moe_W.g2)
+        self.moe_x, self.moe_ids, self.moe_w = mc.x, mc.topk_ids, mc.topk_w
+        self.moe_out = torch.empty(MOE_T, H, dtype=torch.bfloat16, device=dev)
+        self.moe_ws = torch.empty(nv.nvfp4_moe_workspace(MOE_T, H, I, E, topk), dtype=torch.uint8, device=dev)
+        self.moe_E, self.moe_I, self.moe_H, self.moe_topk = E, I, H, topk
+        self.moe_flops = 2.0 * MOE_T * topk * 3 * H * I
+        self.flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+
+    # --- stages ------------------------------------------------------------
+    def prefill(self):
+        nv = self.nv
+        nv.nvfp4_quantize_act(self.pre_x, self.pre_g, self.pre_codes, self.pre_sf)
+        nv.nvfp4_linear_w4a4(self.pre_codes, self.pre_sf, self.pre_W.codes, self.pre_W.scales, self.pre_alpha,
+                             self.pre_W.N, self.pre_W.K, out=self.pre_out)
+
+    def gemm_only(self):
+        self.nv.nvfp4_linear_w4a4(self.pre_codes, self.pre_sf, self.pre_W.codes, self.pre_W.scales,
+                                  self.pre_alpha, self.pre_W.N, self.pre_W.K, out=self.pre_out)
+
+    def moe(self):
+        self.nv.nvfp4_moe_w4a4(self.moe_x, self.moe_ids, self.moe_w, self.moe_g_a1, self.moe_W.w13_codes,
+                               self.moe_W.w13_sf, self.moe_a13, self.moe_g_a2, self.moe_W.w2_codes,
+                               self.moe_W.w2_sf, self.moe_a2, self.moe_E, self.moe_I, out=self.moe_out,
+                               workspace=self.moe_ws)
+
+    def build_decode_graphs(self):
+        lib = self.lib
+        for d in self.decode:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+
+            def call(j, d=d, stream=None):
+                st = lib.nvfp4_linear_w4a16(
+                    ctypes.c_void_p(d["x"].data_ptr()), d["T"], d["K"], ctypes.c_void_p(d["codes"][j].data_ptr()),
+                    ctypes.c_void_p(d["scales"][j].data_ptr()), d["N"], d["K"], ctypes.c_void_p(d["alpha"].data_ptr()),
+                    ctypes.c_void_p(d["out"].data_ptr()), d["N"], ctypes.c_void_p(d["ws"].data_ptr()),
+                    d["ws"].numel(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+                if st != 0:
+                    raise RuntimeError(f"nvfp4_linear_w4a16 status {st}")
+            with torch.cuda.stream(s):
+                call(0)
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for j in range(d["ncopy"]):
+                    call(j)
+            d["graph"] = g
+        torch.cuda.synchronize()
+
+    def flush(self):
+        self.flush_buf.fill_(1)
+
+    def launches_per_step(self) -> int:
+        return 2 + sum(d["ncopy"] * d["launches"] for d in self.decode) + 7
+
+
+def _timed(fn, stream):
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    fn()
+    b.record(stream)
+    return a, b
+
+
+def run_ours(args, world, rank, local):
+    import nvfp4_block_scaled_act_gb300 as nv
+    from nvfp4_block_scaled_act_gb300 import build
+    build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wl = Workload(dev, nv)
+    wl.build_decode_graphs()
+    stream = torch.cuda.current_stream()
+
+    def step(record):
+        wl.flush()
+        ev_pre = _timed(wl.prefill, stream)
+        wl.flush()
+        ev_gemm = _timed(wl.gemm_only, stream)
+        dec = []
+        for d in wl.decode:
+            wl.flush()
+            dec.append(_timed(d["graph"].replay, stream))
+        wl.flush()
+        ev_moe = _timed(wl.moe, stream)
+        if record is not None:
+            record.append((ev_pre, ev_gemm, dec, ev_moe))
+
+    for _ in range(args.warmup):
+        step(None)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    recs = []
+    with ClockSampler(local) as clocks:
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step(recs)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    # device times
+    ms = lambda ev: ev[0].elapsed_time(ev[1])  # noqa: E731
+    pre_ms = [ms(r[0]) for r in recs]
+    gemm_ms = [ms(r[1]) for r in recs]
+    moe_ms = [ms(r[3]) for r in recs]
+    dec_ms = [[ms(e) for e in r[2]] for r in recs]
+    step_ms = [p + g + sum(d) + m for p, g, d, m in zip(pre_ms, gemm_ms, dec_ms, moe_ms)]
+    t_pre = statistics.median(pre_ms) * 1e-3
+    t_gemm = statistics.median(gemm_ms) * 1e-3
+    t_moe = statistics.median(moe_ms) * 1e-3
+    per_step = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([t_pre, per_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_pre, per_step = float(t[0]), float(t[1])
+    hbm, bf16, bf16_sus, peak_src = _peaks()
+    fp4_peak = bf16 * FP4_OVER_BF16
+    decode = {}
+    for i, d in enumerate(wl.decode):
+        t = statistics.median([x[i] for x in dec_ms]) * 1e-3 / d["ncopy"]
+        decode[f"T{d['T']}_{d['N']}x{d['K']}"] = {
+            "us": round(t * 1e6, 3), "gbs": round(d["bytes"] / t / 1e9, 1),
+            "frac_hbm": round(d["bytes"] / t / 1e9 / hbm, 4)}
+    value = world * wl.pre_flops / t_pre / 1e12
+    gemm_tflops = wl.pre_flops / t_gemm / 1e12
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(per_step, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, ue4m3 block scales) -> fp32 accumulate",
+        "data": "synthetic (seeded N(0,1) activations with 1% outlier channels x20, N(0,0.02) weights)",
+        "config": {"workload": "fused qkv W4A4 prefill M=8192 N=5120+1024+1024 K=5120 (quant + GEMM)",
+                   "decode": "W4A16 T=1..16 on 8704x5120 and 5120x4352, cold weights in CUDA graphs",
+                   "moe": "W4A4 MoE E=128 top8 H=2048 I=768 T=4096",
+                   "l2": "flushed (256 MiB write) before every stage, outside the timed events",
+                   "parallelism": f"replicas x{world}"},
+        "prefill": {"ms": round(t_pre * 1e3, 4), "tflops": round(wl.pre_flops / t_pre / 1e12, 1),
+                    "frac_fp4_peak": round(wl.pre_flops / t_pre / 1e12 / fp4_peak, 4)},
+        "gemm_w4a4": {"ms": round(t_gemm * 1e3, 4), "tflops": round(gemm_tflops, 1),
+                      "frac_fp4_peak": round(gemm_tflops / fp4_peak, 4)},
+        "decode": decode,
+        "moe": {"ms": round(t_moe * 1e3, 4), "tflops": round(wl.moe_flops / t_moe / 1e12, 1),
+                "frac_fp4_peak": round(wl.moe_flops / t_moe / 1e12 / fp4_peak, 4)},
+        "roofline": {"kernel": "gemm_nvfp4_kernel (W4A4, M=8192)", "bound": "tensor",
+                     "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / fp4_peak, 4),
+                     "peak_source": f"{peak_src} bf16 burst {bf16} TFLOP/s x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
+                     "algorithmic_bytes": wl.pre_bytes, "traffic": None},
+        "gpu_launches": wl.launches_per_step() * args.steps,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    clk = clocks.summary()
+    result["clocks"] = {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]}
+    # end to end through the public API: pinned host input -> device -> quant + GEMM -> host output
+    result["e2e"] = e2e_prefill(wl, nv, dev, args)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def e2e_prefill(wl, nv, dev, args):
+    M, N, K = PREFILL_M, wl.pre_W.N, wl.pre_W.K
+    x_host = wl.pre_x.cpu().pin_memory()
+    out_host = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(wl.pre_x)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        x_dev.copy_(x_host, non_blocking=True)
+        nv.nvfp4_quantize_act(x_dev, wl.pre_g, wl.pre_codes, wl.pre_sf)
+        nv.nvfp4_linear_w4a4(wl.pre_codes, wl.pre_sf, wl.pre_W.codes, wl.pre_W.scales, wl.pre_alpha, N, K,
+                             out=wl.pre_out)
+        out_host.copy_(wl.pre_out, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        one()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        a, b = _timed(one, stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3)
+    t = statistics.median(ts)
+    return {"value": round(wl.pre_flops / t / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_prefill_setup(rows):
+    import oracle
+    case = synthdata.prefill_case(rows, seed=0)
+    wc, ws, g_w, _ = oracle.quantize_weight_parts(case.w_parts)
+    g_a = oracle.global_scale(case.x_calib)
+    return oracle, case, wc, ws, g_w, g_a
+
+
+def cpu_baseline(seconds: float):
+    """The oracle (as it stands) on a bounded sample of the prefill: quantise
+    `rows` activation rows and run the W4A4 GEMM against the full fused weight."""
+    ora, case, wc, ws, g_w, g_a = _oracle_prefill_setup(64)
+    N, K = case.N, case.K
+    threads = ora.threads()
+    t0 = time.perf_counter()
+    ac, asf = ora.quantize(case.x, g_a)
+    ora.linear_w4a4(ac, asf, 64, wc, ws, N, K, ora.alpha_w4a4(g_a, g_w))
+    t1 = time.perf_counter() - t0
+    rows = int(max(64, min(PREFILL_M, 64 * seconds / max(t1, 1e-3))))
+    rows = (rows // 64) * 64
+    ora2, case2, wc2, ws2, g_w2, g_a2 = _oracle_prefill_setup(rows)
+    t0 = time.perf_counter()
+    ac, asf = ora2.quantize(case2.x, g_a2)
+    ora2.linear_w4a4(ac, asf, rows, wc2, ws2, N, K, ora2.alpha_w4a4(g_a2, g_w2))
+    t = time.perf_counter() - t0
+    flops = 2.0 * rows * N * K
+    return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} of {PREFILL_M} prefill rows (quantise + W4A4 against the full 7168x5120 weight), "
+                      f"{t:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    threads = oracle.threads()
+    ora, case, wc, ws, g_w, g_a = _oracle_prefill_setup(64)
+    N, K = case.N, case.K
+    # size the per-step sample so the whole run stays within a few minutes
+    t0 = time.perf_counter()
+    ac, asf = ora.quantize(case.x, g_a)
+    ora.linear_w4a4(ac, asf, 64, wc, ws, N, K, ora.alpha_w4a4(g_a, g_w))
+    t64 = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    rows = int(max(16, min(PREFILL_M, 64 * budget / max(t64, 1e-3))) // 16 * 16)
+    case = synthdata.prefill_case(rows, seed=0)
+    alpha = ora.alpha_w4a4(g_a, g_w)
+
+    def step():
+        a, s = ora.quantize(case.x, g_a)
+        ora.linear_w4a4(a, s, rows, wc, ws, N, K, alpha)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    t = (time.perf_counter() - t0) / args.steps
+    flops = 2.0 * rows * N * K
+    v = flops / t / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (CPU oracle, IEEE)", "data": "synthetic",
+        "config": {"workload": "fused qkv W4A4 prefill M=8192 N=5120+1024+1024 K=5120 (quant + GEMM)",
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} of {PREFILL_M} prefill rows per step"},
+        "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -75,6 +75,29 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                : "memory");
 }
 
+// 32 fp32 accumulator values * alpha -> bf16, stored as four 16-byte vectors;
+// `remaining` = valid columns from dst on (a multiple of 8).
+__device__ __forceinline__ void store_bf16_32(uint16_t* dst, const uint32_t (&r)[32], float alpha, int remaining) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    if (8 * v < remaining) {
+      uint4 o;
+      o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * alpha, __uint_as_float(r[8 * v + 1]) * alpha);
+      o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * alpha, __uint_as_float(r[8 * v + 3]) * alpha);
+      o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * alpha, __uint_as_float(r[8 * v + 5]) * alpha);
+      o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * alpha, __uint_as_float(r[8 * v + 7]) * alpha);
+      *reinterpret_cast<uint4*>(dst + 8 * v) = o;
+    }
+  }
+}
+
+__device__ __forceinline__ void red_add_32(float* dst, const uint32_t (&r)[32], float scale) {
+#pragma unroll
+  for (int v = 0; v < 8; ++v)
+    red_add_v4(dst + 4 * v, __uint_as_float(r[4 * v]) * scale, __uint_as_float(r[4 * v + 1]) * scale,
+               __uint_as_float(r[4 * v + 2]) * scale, __uint_as_float(r[4 * v + 3]) * scale);
+}
+
 // Quantise 64 consecutive h values (four 16-blocks) of one row: 32 code bytes
 // and 4 scale bytes.
 __device__ __forceinline__ void quant64(const float (&h)[64], float g, uint4& c0, uint4& c1, uint32_t& s4) {
@@ -221,6 +244,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_nvfp4(128, BN);
+      // Descriptors of stage 0; stage s adds s * STAGE_BYTES / 16 to the
+      // 14-bit address field (all of shared memory stays below 256 KB).
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t da0 = desc_kmajor_sw128(sbase);
+      const uint64_t db0 = desc_kmajor_sw128(sbase + Cfg::A_BYTES);
+      const uint64_t dsa0 = desc_scale_atom(sbase + Cfg::A_BYTES + Cfg::B_BYTES);
+      const uint64_t dsb0 = desc_scale_atom(sbase + Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES);
+      const uint32_t tsf0 = tmem_base + Cfg::SF_BASE;
+      constexpr uint32_t kStageUnits = Cfg::STAGE_BYTES >> 4;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -233,22 +265,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             break;
           }
           tc_fence_after();
-          const int ks = min(4, (p.K - kb * 256) / 64);
-          const uint32_t sA = smem_u32(smem + stage * Cfg::STAGE_BYTES);
-          const uint32_t sB = sA + Cfg::A_BYTES;
-          const uint32_t sSFA = sB + Cfg::B_BYTES;
-          const uint32_t sSFB = sSFA + Cfg::SFA_BYTES;
-          const uint32_t t_sfa = tmem_base + Cfg::SF_BASE + stage * Cfg::SF_COLS;
+          const int ks = min(4, (p.K - kb * 256) >> 6);
+          const uint64_t off = static_cast<uint64_t>(stage * kStageUnits);
+          const uint64_t da = da0 + off, db = db0 + off, dsa = dsa0 + off, dsb = dsb0 + off;
+          const uint32_t t_sfa = tsf0 + stage * Cfg::SF_COLS;
           const uint32_t t_sfb = t_sfa + 16;
-          for (int s = 0; s < ks; ++s) {
-            tmem_cp_32x128b_x4(t_sfa + 4 * s, desc_scale_atom(sSFA + 512 * s));
 #pragma unroll
-            for (int j = 0; j < Cfg::NBLK; ++j)
-              tmem_cp_32x128b_x4(t_sfb + (BN / 32) * s + 4 * j, desc_scale_atom(sSFB + j * 2048 + 512 * s));
+          for (int s = 0; s < 4; ++s) {
+            if (s < ks) {
+              tmem_cp_32x128b_x4(t_sfa + 4 * s, dsa + 32 * s);
+#pragma unroll
+              for (int j = 0; j < Cfg::NBLK; ++j)
+                tmem_cp_32x128b_x4(t_sfb + (BN / 32) * s + 4 * j, dsb + 128 * j + 32 * s);
+            }
           }
-          for (int s = 0; s < ks; ++s) {
-            umma_nvfp4(d_tmem, desc_kmajor_sw128(sA + 32 * s), desc_kmajor_sw128(sB + 32 * s), idesc,
-                       t_sfa + 4 * s, t_sfb + (BN / 32) * s, (kb > 0 || s > 0) ? 1u : 0u);
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            if (s < ks)
+              umma_nvfp4(d_tmem, da + 2 * s, db + 2 * s, idesc, t_sfa + 4 * s, t_sfb + (BN / 32) * s,
+                         (kb > 0 || s > 0) ? 1u : 0u);
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == STAGES) {
@@ -286,31 +321,28 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
 
       if constexpr (MODE == kEpiDense) {
-        constexpr int COLS = BN / PARTS;
-        const int m = mt * 128 + row;
-        for (int c0 = part * COLS; c0 < (part + 1) * COLS; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + c0, r);
-          tmem_ld_wait();
-          const int n0 = nt * BN + c0;
-          if (m < p.M) {
-            uint16_t* dst = p.out + static_cast<int64_t>(m) * p.ldo + n0;
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              if (n0 + 8 * v < p.N) {
-                uint4 o;
-                o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * alpha_dense, __uint_as_float(r[8 * v + 1]) * alpha_dense);
-                o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * alpha_dense, __uint_as_float(r[8 * v + 3]) * alpha_dense);
-                o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * alpha_dense, __uint_as_float(r[8 * v + 5]) * alpha_dense);
-                o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * alpha_dense, __uint_as_float(r[8 * v + 7]) * alpha_dense);
-                *reinterpret_cast<uint4*>(dst + 8 * v) = o;
-              }
-            }
-          }
-        }
+        // this warp owns 128 accumulator columns: read them all, release the
+        // accumulator, then convert and store
+        static_assert(BN / PARTS == 128, "dense epilogue: 128 columns per warp");
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        const uint32_t tc = t_row + part * 128;
+        tmem_ld_32x32b_x32(tc, r0);
+        tmem_ld_32x32b_x32(tc + 32, r1);
+        tmem_ld_32x32b_x32(tc + 64, r2);
+        tmem_ld_32x32b_x32(tc + 96, r3);
+        tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acce_bar[acc]);
+        const int m = mt * 128 + row;
+        if (m < p.M) {
+          const int nbase = nt * BN + part * 128;
+          uint16_t* dst = p.out + static_cast<int64_t>(m) * p.ldo + nbase;
+          store_bf16_32(dst, r0, alpha_dense, p.N - nbase);
+          store_bf16_32(dst + 32, r1, alpha_dense, p.N - nbase - 32);
+          store_bf16_32(dst + 64, r2, alpha_dense, p.N - nbase - 64);
+          store_bf16_32(dst + 96, r3, alpha_dense, p.N - nbase - 96);
+        }
       } else if constexpr (MODE == kEpiGatedQuant || MODE == kEpiGatedAmax) {
         // accumulator columns [0, 128) = gate, [128, 256) = up; this warp owns
         // h columns [64 * part, 64 * part + 64)
@@ -357,30 +389,28 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
       } else {
         // routed down projection: y[t, n] += w_route * alpha_e * acc
-        const int prow = mt * 128 + row;
-        const int rm = p.row_map[prow];
-        const int e = p.tile_expert[mt];
-        float scale = 0.0f;
-        float* dst = nullptr;
-        if (rm >= 0) {
-          scale = __fmul_rn(__ldg(p.topk_w + rm), __ldg(p.alpha + e));
-          dst = p.y + static_cast<int64_t>(rm / p.topk) * p.ldy + nt * BN;
-        }
-        constexpr int COLS = BN / PARTS;
-        for (int c0 = part * COLS; c0 < (part + 1) * COLS; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + c0, r);
-          tmem_ld_wait();
-          if (rm >= 0) {
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              red_add_v4(dst + c0 + 4 * v, __uint_as_float(r[4 * v]) * scale, __uint_as_float(r[4 * v + 1]) * scale,
-                         __uint_as_float(r[4 * v + 2]) * scale, __uint_as_float(r[4 * v + 3]) * scale);
-          }
-        }
+        static_assert(BN / PARTS == 128, "down epilogue: 128 columns per warp");
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        const uint32_t tc = t_row + part * 128;
+        tmem_ld_32x32b_x32(tc, r0);
+        tmem_ld_32x32b_x32(tc + 32, r1);
+        tmem_ld_32x32b_x32(tc + 64, r2);
+        tmem_ld_32x32b_x32(tc + 96, r3);
+        tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acce_bar[acc]);
+        const int prow = mt * 128 + row;
+        const int rm = p.row_map[prow];
+        if (rm >= 0) {
+          const int e = p.tile_expert[mt];
+          const float scale = __fmul_rn(__ldg(p.topk_w + rm), __ldg(p.alpha + e));
+          float* dst = p.y + static_cast<int64_t>(rm / p.topk) * p.ldy + nt * BN + part * 128;
+          red_add_32(dst, r0, scale);
+          red_add_32(dst + 32, r1, scale);
+          red_add_32(dst + 64, r2, scale);
+          red_add_32(dst + 96, r3, scale);
+        }
       }
       if (++acc == NUM_ACC) {
         acc = 0;
@@ -400,7 +430,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-using DenseCfg = GemmCfg<128, 2, 6, 4, kEpiDense>;
+using DenseCfg = GemmCfg<256, 1, 4, 8, kEpiDense>;
 using GatedCfg = GemmCfg<256, 1, 4, 8, kEpiGatedQuant>;
 using AmaxCfg = GemmCfg<256, 1, 4, 8, kEpiGatedAmax>;
 using DownCfg = GemmCfg<128, 2, 6, 4, kEpiDownSum>;
