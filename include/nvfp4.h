@@ -142,6 +142,28 @@ nvfp4_status nvfp4_linear_w4a16(const void* x_bf16, int64_t T, int64_t ldx,
                                 const float* d_alpha, void* out_bf16, int64_t ldo,
                                 void* workspace, size_t ws_bytes, nvfp4_stream_t stream);
 
+/* The same W4A16 decode GEMM for callers that cannot allocate device memory
+ * (a runtime that owns the whole GPU through its own pool, code already inside
+ * CUDA stream capture, a plugin host that hands out only inputs and outputs).
+ * The pages have no counterpart of this call; it is an addition of this
+ * library.  Instead of a caller-sized workspace it keeps the split-K partial
+ * sums in one 6 MiB array compiled into the library, which every GPU that
+ * loads the library holds until the process exits.  It allocates nothing.
+ *   - Arguments, layouts and results are those of nvfp4_linear_w4a16.
+ *   - Shapes whose partials need more than 6 MiB (split-K partials of
+ *     splits * T * N fp32; e.g. T = 16, N = 25600, K = 4096) are refused with
+ *     NVFP4_ERR_WORKSPACE_TOO_SMALL; both decode shapes of the workloads fit.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array and it keeps the last call's partials;
+ *     nothing in it needs to start at zero (each partial is written before it
+ *     is read).  Calls that overlap on the GPU (other streams, other threads)
+ *     race on the array: serialise them. */
+nvfp4_status nvfp4_linear_w4a16_noalloc(const void* x_bf16, int64_t T, int64_t ldx,
+                                        const uint8_t* w_codes, const uint8_t* w_sf, int64_t N,
+                                        int64_t K, const float* d_alpha, void* out_bf16,
+                                        int64_t ldo, nvfp4_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Mixture of experts, W4A4 (the W4A4 MoE prefill page, Changes; layer flow
  * align -> gate_up -> act -> down -> sum of "speed up the nvfp4 moe prefill

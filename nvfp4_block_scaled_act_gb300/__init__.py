@@ -59,6 +59,7 @@ SIGNATURES = {
     "nvfp4_linear_w4a4": (_ST, [_P, _P, _I64, _P, _P, _I64, _I64, _P, _P, _I64, _P]),
     "nvfp4_linear_w4a16_workspace": (_SZ, [_I64, _I64, _I64]),
     "nvfp4_linear_w4a16": (_ST, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, _I64, _P, _SZ, _P]),
+    "nvfp4_linear_w4a16_noalloc": (_ST, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, _I64, _P]),
     "nvfp4_moe_workspace": (_SZ, [_I64, _I64, _I64, _I64, _I]),
     "nvfp4_moe_workspace_layout": (_ST, [_I64, _I64, _I64, _I64, _I, ctypes.POINTER(MoELayout)]),
     "nvfp4_moe_w4a4": (_ST, [_P, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P,

@@ -275,3 +275,83 @@ cudaError_t launch_gemv_w4a16(const void* x, int64_t T, int64_t ldx, const uint8
 }
 
 }  // namespace nvfp4
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the W4A16 decode GEMM.
+//
+// Some callers cannot allocate device memory when they run a decode GEMM: a
+// runtime that owns every byte of the GPU through its own pool and forbids
+// side allocations, code already running inside stream capture of a CUDA
+// graph where a cudaMalloc would break the capture, or a plugin host that
+// hands out only its inputs and outputs.  For them this entry point keeps the
+// split-K partial sums in a fixed array compiled into the library instead of
+// a caller-sized workspace.  The array lives in every GPU that loads the
+// library until the process exits.  In host code its name is only a stand-in
+// for the device array, so the device address is looked up once per device
+// (with that device current) and passed to the kernels.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+#include "nvfp4.h"
+
+namespace nvfp4 {
+
+constexpr size_t kStaticScratchBytes = size_t(6) << 20;  // 6 MiB of fp32 partials
+static __device__ __align__(256) float g_w4a16_static_scratch[kStaticScratchBytes / sizeof(float)];
+
+namespace {
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_static_mu;
+float* g_static_ptr[kMaxScratchDevices] = {};
+int g_static_sms[kMaxScratchDevices] = {};
+
+// Device address of the static scratch on the current device (looked up on
+// the first call per device) and that device's SM count.
+nvfp4_status static_scratch(float** ptr, int* sms) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return NVFP4_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    int major = 0, minor = 0, count = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    if (major != 10 || minor != 3) return NVFP4_ERR_NO_DEVICE;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_w4a16_static_scratch) != cudaSuccess || p == nullptr) return NVFP4_ERR_CUDA;
+    g_static_ptr[dev] = static_cast<float*>(p);
+    g_static_sms[dev] = count;
+  }
+  *ptr = g_static_ptr[dev];
+  *sms = g_static_sms[dev];
+  return NVFP4_OK;
+}
+}  // namespace
+
+}  // namespace nvfp4
+
+extern "C" nvfp4_status nvfp4_linear_w4a16_noalloc(const void* x, int64_t T, int64_t ldx, const uint8_t* w_codes,
+                                                   const uint8_t* w_sf, int64_t N, int64_t K, const float* d_alpha,
+                                                   void* out, int64_t ldo, nvfp4_stream_t stream) {
+  using namespace nvfp4;
+  if (T < 0 || N <= 0 || K <= 0 || ldx < K || ldo < N) return NVFP4_ERR_INVALID_ARG;
+  if (T > 16 || N % 8 != 0 || K % 128 != 0 || N > (1LL << 30) || K > (1LL << 24))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return NVFP4_OK;
+  if (!x || !w_codes || !w_sf || !d_alpha || !out) return NVFP4_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(w_codes) & 15u) ||
+      (reinterpret_cast<uintptr_t>(w_sf) & 15u) || (ldx % 8) != 0 || (ldo % 2) != 0 ||
+      (reinterpret_cast<uintptr_t>(out) & 3u))
+    return NVFP4_ERR_MISALIGNED;
+  float* scratch = nullptr;
+  int sms = 0;
+  const nvfp4_status st = static_scratch(&scratch, &sms);
+  if (st != NVFP4_OK) return st;
+  const GemvPlan plan = gemv_plan(T, N, K, sms);
+  if (plan.ws_bytes > kStaticScratchBytes) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
+  return launch_gemv_w4a16(x, T, ldx, w_codes, w_sf, N, K, d_alpha, out, ldo, plan.ws_bytes ? scratch : nullptr,
+                           plan, stream) == cudaSuccess
+             ? NVFP4_OK
+             : NVFP4_ERR_CUDA;
+}
