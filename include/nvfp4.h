@@ -86,14 +86,14 @@ nvfp4_status nvfp4_make_alpha(const float* d_g_a, const float* d_g_w, int64_t n,
                               nvfp4_stream_t stream);
 
 /* *d_out = max over i < n of d_in[i] (fp32).  Used for the fused-weight global
- * ("a fused weight uses its largest per-part global", "run nvfp4 linears ...",
- * Changes) and the MoE input global ("each GEMM input uses the max over the
- * layer's experts", the W4A4 MoE prefill page, Changes). */
+ * (a fused weight takes the largest of its parts' globals: "run nvfp4 linears
+ * ...", Changes) and the MoE input globals (the largest per-expert input
+ * global feeds each GEMM: the W4A4 MoE prefill page, Changes). */
 nvfp4_status nvfp4_reduce_max(const float* d_in, int64_t n, float* d_out, nvfp4_stream_t stream);
 
 /* NVFP4 quantisation of bf16 activations (or weights) with a static global
- * ("run nvfp4 linears ...", Changes: the activation quant kernel, rows split
- * into blocks, 128x4-swizzled scales).  Per 16-element block of a row:
+ * ("run nvfp4 linears ...", Changes: the activation quantiser, which cuts long
+ * rows into chunks and writes 128x4-swizzled scales).  Per 16-element block of a row:
  * amax -> s = E4M3_satfinite((amax / 6) * g) -> codes = e2m1_satfinite(x * (g / s)),
  * all codes +0 when s == 0.
  *   x_bf16  [M, K] bf16, row stride ldx >= K elements, ldx % 8 == 0

@@ -3,8 +3,9 @@
 // ("Add BF16_FP4 GEMM ... for W4A16 workloads", section "Summary":
 // out = (a @ dequant(b, b_sf).T) * alpha; the small-batch W4A16 kernels of
 // "run nvfp4 linears on nvfp4 activations on sm_120", section "Changes":
-// weight rows on one MMA side, tokens on the other, a fixed permutation of k
-// inside each 128-k block so that plain 16-byte code loads are the fragments;
+// one MMA operand carries weight rows and the other the tokens, and k is
+// reordered inside 128-element blocks until a single 16-byte load of codes
+// already is an MMA operand fragment;
 // split-K with a fixed-order reduce, as in the FlashInfer follow-up).
 //
 // HBM-bound: every weight byte is read once, with 16-byte non-allocating loads.

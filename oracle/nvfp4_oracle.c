@@ -148,7 +148,8 @@ uint8_t nvo_f32_to_e2m1_satfinite(float f) {
 }
 
 /* ------------------------------------------------------------------------- */
-/* 128x4-swizzled block-scale layout ([linear] "128x4-swizzled block scales";  */
+/* 128x4-swizzled block-scale layout ([linear] Changes: the block scales of  */
+/* the weight are stored 128x4-swizzled;                                      */
 /* [mmbf16] SfLayout.layout_128x4).  READING: the pages name the layout but    */
 /* print no formula; this is the block-scaling layout scaled_mm consumes: the  */
 /* scale matrix (rows x C) is cut into 128-row x 4-column atoms of 512 bytes,  */
@@ -473,7 +474,7 @@ void nvo_moe_w4a4(const uint16_t* x, int64_t T, int64_t H, int64_t I, int64_t E,
 
 /* ------------------------------------------------------------------------- */
 /* MoE calibration of the second GEMM's input ([moe] "Static activation        */
-/* scales": each GEMM input uses the max over the layer's experts).  READING:  */
+/* scales": the largest per-expert input global feeds each GEMM).  READING:   */
 /* every calibration row goes through every expert (steps 1-3 above), so each  */
 /* expert has a finite amax; amax_out[e] = max |h| over the rows and the I     */
 /* columns.  The caller forms g_a2,e = 2688 / amax_out[e] and takes the max.   */
