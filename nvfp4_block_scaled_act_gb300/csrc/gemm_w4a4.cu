@@ -34,12 +34,11 @@
 
 namespace nvfp4 {
 
-template <int BN_, int NUM_ACC_, int STAGES_, int NE_, int MODE_>
+template <int BN_, int NUM_ACC_, int STAGES_, int MODE_>
 struct GemmCfg {
   static constexpr int BN = BN_;           // MMA N (B rows per tile)
   static constexpr int NUM_ACC = NUM_ACC_;
   static constexpr int STAGES = STAGES_;
-  static constexpr int NE = NE_;           // epilogue warps (multiple of 4)
   static constexpr int MODE = MODE_;
   static constexpr int BM = 128;
   static constexpr int A_BYTES = BM * 128;
@@ -52,12 +51,10 @@ struct GemmCfg {
   static constexpr int SF_COLS = 16 + 4 * (BN / 32);  // TMEM scale columns per stage
   static constexpr int SF_BASE = NUM_ACC * BN;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int THREADS = 64 + 32 * NE;
   static constexpr bool GROUPED = MODE != kEpiDense;
   static_assert(SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(SMEM_BYTES <= 232448, "smem budget");
-  static_assert(NE % 4 == 0, "epilogue warps cover the four TMEM lane quadrants");
 };
 
 // ---------------------------------------------------------------------------
@@ -125,20 +122,36 @@ __device__ __forceinline__ void quant64(const float (&h)[64], float g, uint4& c0
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
+constexpr int kThreads = 512;   // four warpgroups
+constexpr int kNumEpi = 8;      // epilogue warps (warpgroups 2 and 3)
+constexpr int kRegsLow = 56;    // producer / MMA / scale-writer warpgroups
+constexpr int kRegsHigh = 200;  // epilogue warpgroups; 2*128*56 + 2*128*200 = 65536
+
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow)); }
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh)); }
+
+// Read COLS accumulator columns of this warp's 32 lanes into registers.
+template <int COLS>
+__device__ __forceinline__ void drain(uint32_t taddr, uint32_t (&r)[COLS / 32][32]) {
+#pragma unroll
+  for (int c = 0; c < COLS / 32; ++c) tmem_ld_32x32b_x32(taddr + 32 * c, r[c]);
+  tmem_ld_wait();
+}
+
 template <class Cfg>
-__global__ void __launch_bounds__(Cfg::THREADS, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const GemmParams p) {
   constexpr int STAGES = Cfg::STAGES;
   constexpr int NUM_ACC = Cfg::NUM_ACC;
   constexpr int BN = Cfg::BN;
-  constexpr int NE = Cfg::NE;
   constexpr int MODE = Cfg::MODE;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_bar[STAGES];
-  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];   // TMA data landed
+  __shared__ __align__(8) uint64_t sf_bar[STAGES];     // scales written to TMEM
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];  // MMAs of the stage done
   __shared__ __align__(8) uint64_t accf_bar[NUM_ACC];
   __shared__ __align__(8) uint64_t acce_bar[NUM_ACC];
   __shared__ __align__(8) uint64_t done_bar;
@@ -151,11 +164,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
+      mbar_init(&sf_bar[s], 4);
       mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < NUM_ACC; ++a) {
       mbar_init(&accf_bar[a], 1);
-      mbar_init(&acce_bar[a], NE);
+      mbar_init(&acce_bar[a], kNumEpi);
     }
     mbar_init(&done_bar, 1);
     abort_flag = 0;
@@ -176,10 +190,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
   const int m_tiles = Cfg::GROUPED ? *p.d_m_tiles : p.m_tiles;
   const int total = m_tiles * p.n_tiles;
+  const int wg = warp >> 2;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (wg == 0) {
+    regs_dec();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- producer
       uint32_t stage = 0, phase = 0;
       uint32_t last_phase[STAGES];
       bool issued[STAGES];
@@ -239,77 +255,122 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
       for (int s = 0; s < STAGES; ++s)
         if (issued[s]) mbar_wait(&full_bar[s], last_phase[s], reinterpret_cast<volatile int*>(&drain_abort), p.status);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_nvfp4(128, BN);
-      // Descriptors of stage 0; stage s adds s * STAGE_BYTES / 16 to the
-      // 14-bit address field (all of shared memory stays below 256 KB).
-      const uint32_t sbase = smem_u32(smem);
-      const uint64_t da0 = desc_kmajor_sw128(sbase);
-      const uint64_t db0 = desc_kmajor_sw128(sbase + Cfg::A_BYTES);
-      const uint64_t dsa0 = desc_scale_atom(sbase + Cfg::A_BYTES + Cfg::B_BYTES);
-      const uint64_t dsb0 = desc_scale_atom(sbase + Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES);
-      const uint32_t tsf0 = tmem_base + Cfg::SF_BASE;
-      constexpr uint32_t kStageUnits = Cfg::STAGE_BYTES >> 4;
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1, &abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.kblocks; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, &abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        const uint32_t idesc = idesc_nvfp4(128, BN);
+        // Descriptors of stage 0; stage s adds s * STAGE_BYTES / 16 to the
+        // 14-bit address field (all of shared memory stays below 256 KB).
+        const uint32_t sbase = smem_u32(smem);
+        const uint64_t da0 = desc_kmajor_sw128(sbase);
+        const uint64_t db0 = desc_kmajor_sw128(sbase + Cfg::A_BYTES);
+        const uint32_t tsf0 = tmem_base + Cfg::SF_BASE;
+        constexpr uint32_t kStageUnits = Cfg::STAGE_BYTES >> 4;
+        uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+          if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1, &abort_flag, p.status)) break;
           tc_fence_after();
-          const int ks = min(4, (p.K - kb * 256) >> 6);
-          const uint64_t off = static_cast<uint64_t>(stage * kStageUnits);
-          const uint64_t da = da0 + off, db = db0 + off, dsa = dsa0 + off, dsb = dsb0 + off;
-          const uint32_t t_sfa = tsf0 + stage * Cfg::SF_COLS;
-          const uint32_t t_sfb = t_sfa + 16;
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          for (int kb = 0; kb < p.kblocks; ++kb) {
+            if (!mbar_wait(&sf_bar[stage], phase, &abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int ks = min(4, (p.K - kb * 256) >> 6);
+            const uint64_t off = static_cast<uint64_t>(stage * kStageUnits);
+            const uint64_t da = da0 + off, db = db0 + off;
+            const uint32_t t_sfa = tsf0 + stage * Cfg::SF_COLS;
+            const uint32_t t_sfb = t_sfa + 16;
 #pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            if (s < ks) {
-              tmem_cp_32x128b_x4(t_sfa + 4 * s, dsa + 32 * s);
-#pragma unroll
-              for (int j = 0; j < Cfg::NBLK; ++j)
-                tmem_cp_32x128b_x4(t_sfb + (BN / 32) * s + 4 * j, dsb + 128 * j + 32 * s);
+            for (int s = 0; s < 4; ++s) {
+              if (s < ks)
+                umma_nvfp4(d_tmem, da + 2 * s, db + 2 * s, idesc, t_sfa + 4 * s, t_sfb + (BN / 32) * s,
+                           (kb > 0 || s > 0) ? 1u : 0u);
+            }
+            umma_commit(&empty_bar[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
             }
           }
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            if (s < ks)
-              umma_nvfp4(d_tmem, da + 2 * s, db + 2 * s, idesc, t_sfa + 4 * s, t_sfb + (BN / 32) * s,
-                         (kb > 0 || s > 0) ? 1u : 0u);
-          }
-          umma_commit(&empty_bar[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
+          if (!ok) break;
+          umma_commit(&accf_bar[acc]);
+          if (++acc == NUM_ACC) {
+            acc = 0;
+            acc_phase ^= 1;
           }
         }
-        if (!ok) break;
-        umma_commit(&accf_bar[acc]);
-        if (++acc == NUM_ACC) {
-          acc = 0;
-          acc_phase ^= 1;
+        // wait until every MMA issued above has completed
+        umma_commit(&done_bar);
+        int drain_abort = 0;
+        mbar_wait(&done_bar, 0, reinterpret_cast<volatile int*>(&drain_abort), p.status);
+      }
+      __syncwarp();
+    }
+  } else if (wg == 1) {
+    // ------------------------------------------------------------ scale writers
+    // Warp q writes the scale atoms of each landed stage into its own TMEM lane
+    // quadrant: atom row `lane` (16 bytes) -> 4 consecutive columns, the same
+    // replicated layout a 32x128b.warpx4 copy produces, which the block-scaled
+    // MMA reads (column base + row / 32, lane row % 32).
+    regs_dec();
+    const int q = warp & 3;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int kb = 0; kb < p.kblocks; ++kb) {
+        if (!mbar_wait(&full_bar[stage], phase, &abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sSFA = smem + stage * Cfg::STAGE_BYTES + Cfg::A_BYTES + Cfg::B_BYTES;
+        const uint8_t* sSFB = sSFA + Cfg::SFA_BYTES;
+        const uint32_t t_sf = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + Cfg::SF_BASE + stage * Cfg::SF_COLS;
+        uint32_t va[16];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const uint4 x = *reinterpret_cast<const uint4*>(sSFA + 512 * s + 16 * lane);
+          va[4 * s] = x.x;
+          va[4 * s + 1] = x.y;
+          va[4 * s + 2] = x.z;
+          va[4 * s + 3] = x.w;
+        }
+        tmem_st_32x32b_x16(t_sf, va);
+#pragma unroll
+        for (int h = 0; h < Cfg::NBLK; ++h) {  // 16 columns at a time
+          uint32_t vb[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            // columns 16 h + 4 i of the SFB region: k-step s, 128-row block j
+            const int col = 16 * h + 4 * i;
+            const int s = col / (BN / 32);
+            const int j = (col % (BN / 32)) / 4;
+            const uint4 x = *reinterpret_cast<const uint4*>(sSFB + j * 2048 + 512 * s + 16 * lane);
+            vb[4 * i] = x.x;
+            vb[4 * i + 1] = x.y;
+            vb[4 * i + 2] = x.z;
+            vb[4 * i + 3] = x.w;
+          }
+          tmem_st_32x32b_x16(t_sf + 16 + 16 * h, vb);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_bar[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
         }
       }
-      // wait until every MMA and copy issued above has completed
-      umma_commit(&done_bar);
-      int drain_abort = 0;
-      mbar_wait(&done_bar, 0, reinterpret_cast<volatile int*>(&drain_abort), p.status);
     }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;
-    const int q = warp & 3;          // TMEM lane quadrant of this warp
-    const int part = ew >> 2;        // column part of this warp within its quadrant
-    constexpr int PARTS = NE / 4;
+    regs_inc();
+    const int ew = warp - 8;
+    const int q = warp & 3;      // TMEM lane quadrant of this warp
+    const int part = ew >> 2;    // column half of this warp within its quadrant
     uint32_t acc = 0, acc_phase = 0;
     const float alpha_dense = (MODE == kEpiDense) ? __ldg(p.alpha) : 0.0f;
     const float g_out = (MODE == kEpiGatedQuant) ? __ldg(p.g_out) : 0.0f;
@@ -320,30 +381,35 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const int row = 32 * q + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
 
-      if constexpr (MODE == kEpiDense) {
-        // this warp owns 128 accumulator columns: read them all, release the
-        // accumulator, then convert and store
-        static_assert(BN / PARTS == 128, "dense epilogue: 128 columns per warp");
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        const uint32_t tc = t_row + part * 128;
-        tmem_ld_32x32b_x32(tc, r0);
-        tmem_ld_32x32b_x32(tc + 32, r1);
-        tmem_ld_32x32b_x32(tc + 64, r2);
-        tmem_ld_32x32b_x32(tc + 96, r3);
-        tmem_ld_wait();
+      if constexpr (MODE == kEpiDense || MODE == kEpiDownSum) {
+        // this warp owns COLS accumulator columns: read them all, release the
+        // accumulator, then finish from registers
+        constexpr int COLS = BN / 2;
+        uint32_t r[COLS / 32][32];
+        drain<COLS>(t_row + part * COLS, r);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acce_bar[acc]);
-        const int m = mt * 128 + row;
-        if (m < p.M) {
-          const int nbase = nt * BN + part * 128;
-          uint16_t* dst = p.out + static_cast<int64_t>(m) * p.ldo + nbase;
-          store_bf16_32(dst, r0, alpha_dense, p.N - nbase);
-          store_bf16_32(dst + 32, r1, alpha_dense, p.N - nbase - 32);
-          store_bf16_32(dst + 64, r2, alpha_dense, p.N - nbase - 64);
-          store_bf16_32(dst + 96, r3, alpha_dense, p.N - nbase - 96);
+        if constexpr (MODE == kEpiDense) {
+          const int m = mt * 128 + row;
+          if (m < p.M) {
+            const int nbase = nt * BN + part * COLS;
+            uint16_t* dst = p.out + static_cast<int64_t>(m) * p.ldo + nbase;
+#pragma unroll
+            for (int c = 0; c < COLS / 32; ++c) store_bf16_32(dst + 32 * c, r[c], alpha_dense, p.N - nbase - 32 * c);
+          }
+        } else {
+          const int prow = mt * 128 + row;
+          const int rm = p.row_map[prow];
+          if (rm >= 0) {
+            const int e = p.tile_expert[mt];
+            const float scale = __fmul_rn(__ldg(p.topk_w + rm), __ldg(p.alpha + e));
+            float* dst = p.y + static_cast<int64_t>(rm / p.topk) * p.ldy + nt * BN + part * COLS;
+#pragma unroll
+            for (int c = 0; c < COLS / 32; ++c) red_add_32(dst + 32 * c, r[c], scale);
+          }
         }
-      } else if constexpr (MODE == kEpiGatedQuant || MODE == kEpiGatedAmax) {
+      } else {
         // accumulator columns [0, 128) = gate, [128, 256) = up; this warp owns
         // h columns [64 * part, 64 * part + 64)
         uint32_t g0[32], g1[32], u0[32], u1[32];
@@ -387,30 +453,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
           if (lane == 0 && m > 0.0f) atomicMax(p.amax + e, __float_as_uint(m));
         }
-      } else {
-        // routed down projection: y[t, n] += w_route * alpha_e * acc
-        static_assert(BN / PARTS == 128, "down epilogue: 128 columns per warp");
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        const uint32_t tc = t_row + part * 128;
-        tmem_ld_32x32b_x32(tc, r0);
-        tmem_ld_32x32b_x32(tc + 32, r1);
-        tmem_ld_32x32b_x32(tc + 64, r2);
-        tmem_ld_32x32b_x32(tc + 96, r3);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acce_bar[acc]);
-        const int prow = mt * 128 + row;
-        const int rm = p.row_map[prow];
-        if (rm >= 0) {
-          const int e = p.tile_expert[mt];
-          const float scale = __fmul_rn(__ldg(p.topk_w + rm), __ldg(p.alpha + e));
-          float* dst = p.y + static_cast<int64_t>(rm / p.topk) * p.ldy + nt * BN + part * 128;
-          red_add_32(dst, r0, scale);
-          red_add_32(dst + 32, r1, scale);
-          red_add_32(dst + 64, r2, scale);
-          red_add_32(dst + 96, r3, scale);
-        }
       }
       if (++acc == NUM_ACC) {
         acc = 0;
@@ -430,10 +472,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-using DenseCfg = GemmCfg<256, 1, 4, 8, kEpiDense>;
-using GatedCfg = GemmCfg<256, 1, 4, 8, kEpiGatedQuant>;
-using AmaxCfg = GemmCfg<256, 1, 4, 8, kEpiGatedAmax>;
-using DownCfg = GemmCfg<128, 2, 6, 4, kEpiDownSum>;
+using DenseCfg = GemmCfg<256, 1, 4, kEpiDense>;
+using GatedCfg = GemmCfg<256, 1, 4, kEpiGatedQuant>;
+using AmaxCfg = GemmCfg<256, 1, 4, kEpiGatedAmax>;
+using DownCfg = GemmCfg<128, 2, 6, kEpiDownSum>;
 
 template <class Cfg>
 static cudaError_t launch_cfg(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {
@@ -444,7 +486,7 @@ static cudaError_t launch_cfg(const GemmMaps& maps, const GemmParams& p, int gri
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_nvfp4_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(maps.a, maps.b, p);
+  gemm_nvfp4_kernel<Cfg><<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(maps.a, maps.b, p);
   return cudaGetLastError();
 }
 
