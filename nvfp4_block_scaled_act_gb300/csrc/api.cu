@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -77,14 +78,30 @@ inline nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// CTAs per cluster that share each 256-row weight tile of the dense W4A4 GEMM
+// through TMA multicast.  Multicast cuts the L2 -> SM traffic of the weight,
+// but every CTA still holds the whole tile in shared memory, and measured on
+// GB300 (M = 512 ... 8192, N = 7168, K = 5120) 2 and 4 gave no gain over 1, so
+// 1 is the default.  NVFP4_DENSE_CLUSTER = 1, 2 or 4 selects another size.
+int dense_cluster(int64_t m_tiles) {
+  static int forced = -1;
+  if (forced < 0) {
+    const char* env = std::getenv("NVFP4_DENSE_CLUSTER");
+    const int v = env ? std::atoi(env) : 0;
+    forced = (v == 1 || v == 2 || v == 4) ? v : 0;
+  }
+  if (forced > 0 && m_tiles >= forced) return forced;
+  return 1;
+}
+
 }  // namespace
 
-bool make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes) {
+bool make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-  cuuint32_t box[2] = {128, 128};
+  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -243,8 +260,10 @@ nvfp4_status nvfp4_linear_w4a4(const uint8_t* a_codes, const uint8_t* a_sf, int6
     return NVFP4_ERR_MISALIGNED;
   const DeviceInfo* dev = device_info();
   if (!dev) return NVFP4_ERR_NO_DEVICE;
+  const int64_t m_tiles = (M + 127) / 128;
+  const int cl = dense_cluster(m_tiles);
   GemmMaps maps;
-  if (!make_codes_map(&maps.a, a_codes, M, K / 2) || !make_codes_map(&maps.b, w_codes, N, K / 2))
+  if (!make_codes_map(&maps.a, a_codes, M, K / 2) || !make_codes_map(&maps.b, w_codes, N, K / 2, cl == 1 ? 128 : 256 / cl))
     return NVFP4_ERR_CUDA;
   GemmParams p{};
   p.sfa = a_sf;
@@ -252,8 +271,8 @@ nvfp4_status nvfp4_linear_w4a4(const uint8_t* a_codes, const uint8_t* a_sf, int6
   p.K = static_cast<int>(K);
   p.kblocks = static_cast<int>((K + 255) / 256);
   p.sf_atoms = static_cast<int>(K / 64);
-  p.n_tiles = static_cast<int>((N + 127) / 128);
-  p.m_tiles = static_cast<int>((M + 127) / 128);
+  p.n_tiles = static_cast<int>((N + 255) / 256);
+  p.m_tiles = static_cast<int>(m_tiles);
   p.b_rows_total = static_cast<int>(N);
   p.alpha = d_alpha;
   p.out = static_cast<uint16_t*>(out);
@@ -261,9 +280,9 @@ nvfp4_status nvfp4_linear_w4a4(const uint8_t* a_codes, const uint8_t* a_sf, int6
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.status = dev->status;
-  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-  const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
-  return cuda_status(launch_gemm(kEpiDense, maps, p, grid, stream));
+  const int64_t units = ((m_tiles + cl - 1) / cl) * p.n_tiles;
+  const int64_t clusters = units < dev->sms / cl ? units : dev->sms / cl;
+  return cuda_status(launch_gemm(kEpiDense, maps, p, static_cast<int>(clusters * cl), stream, cl));
 }
 
 size_t nvfp4_linear_w4a16_workspace(int64_t T, int64_t N, int64_t K) {

@@ -34,12 +34,14 @@
 
 namespace nvfp4 {
 
-template <int BN_, int NUM_ACC_, int STAGES_, int MODE_>
+template <int BN_, int NUM_ACC_, int STAGES_, int MODE_, int CL_ = 1>
 struct GemmCfg {
   static constexpr int BN = BN_;           // MMA N (B rows per tile)
   static constexpr int NUM_ACC = NUM_ACC_;
   static constexpr int STAGES = STAGES_;
   static constexpr int MODE = MODE_;
+  static constexpr int CL = CL_;           // CTAs of a cluster sharing one B tile (multicast)
+  static constexpr int SLICE = BN_ / CL_;  // B rows each CTA of the cluster loads
   static constexpr int BM = 128;
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
@@ -55,6 +57,7 @@ struct GemmCfg {
   static_assert(SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(SMEM_BYTES <= 232448, "smem budget");
+  static_assert(CL == 1 || (MODE == kEpiDense && SLICE % 64 == 0 && CL <= 4), "multicast: dense tiles only");
 };
 
 // ---------------------------------------------------------------------------
@@ -124,8 +127,8 @@ __device__ __forceinline__ void quant64(const float (&h)[64], float g, uint4& c0
 // ---------------------------------------------------------------------------
 constexpr int kThreads = 512;   // four warpgroups
 constexpr int kNumEpi = 8;      // epilogue warps (warpgroups 2 and 3)
-constexpr int kRegsLow = 56;    // producer / MMA / scale-writer warpgroups
-constexpr int kRegsHigh = 200;  // epilogue warpgroups; 2*128*56 + 2*128*200 = 65536
+constexpr int kRegsLow = 64;    // producer / MMA / scale-writer warpgroups
+constexpr int kRegsHigh = 192;  // epilogue warpgroups; 2*128*64 + 2*128*192 = 65536
 
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow)); }
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh)); }
@@ -165,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&sf_bar[s], 4);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], Cfg::CL);
     }
     for (int a = 0; a < NUM_ACC; ++a) {
       mbar_init(&accf_bar[a], 1);
@@ -185,11 +188,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (Cfg::CL > 1) cluster_sync();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = tmem_slot;
 
+  // Work units: a group of CL consecutive 128-row tiles (one per CTA of the
+  // cluster) times one column tile, column-fastest.
   const int m_tiles = Cfg::GROUPED ? *p.d_m_tiles : p.m_tiles;
-  const int total = m_tiles * p.n_tiles;
+  const int rank = (Cfg::CL > 1) ? static_cast<int>(cluster_ctarank()) : 0;
+  const int total = ((m_tiles + Cfg::CL - 1) / Cfg::CL) * p.n_tiles;
+  const int unit0 = blockIdx.x / Cfg::CL;
+  const int unit_step = gridDim.x / Cfg::CL;
+  constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << Cfg::CL) - 1u);
   const int wg = warp >> 2;
 
   if (wg == 0) {
@@ -205,8 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         last_phase[s] = 0;
       }
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+      for (int tile = unit0; ok && tile < total; tile += unit_step) {
+        const int mg = tile / p.n_tiles, nt = tile - mg * p.n_tiles;
+        const int mt = mg * Cfg::CL + rank;
         const int e = Cfg::GROUPED ? p.tile_expert[mt] : 0;
         int b_row[Cfg::NBLK];
         if (MODE == kEpiDense) {
@@ -226,20 +237,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sB = sA + Cfg::A_BYTES;
           uint8_t* sSFA = sB + Cfg::B_BYTES;
           uint8_t* sSFB = sSFA + Cfg::SFA_BYTES;
-          uint32_t bytes = Cfg::A_BYTES + ks * 512;
+          // bytes landing in this CTA's smem: its own A tile and scales, and the
+          // whole B tile with its scales (from every CTA of the cluster)
+          const bool mvalid = mt < m_tiles;
+          uint32_t bytes = mvalid ? Cfg::A_BYTES + ks * 512 : 0;
 #pragma unroll
           for (int j = 0; j < Cfg::NBLK; ++j)
             if (b_row[j] < p.b_rows_total) bytes += 128 * 128 + ks * 512;
           mbar_arrive_expect_tx(&full_bar[stage], bytes);
-          tma_load_2d(sA, &tmA, &full_bar[stage], kb * 128, mt * 128);
-          bulk_load(sSFA, p.sfa + (static_cast<int64_t>(mt) * p.sf_atoms + kb * 4) * 512, ks * 512,
-                    &full_bar[stage]);
+          if (mvalid) {
+            tma_load_2d(sA, &tmA, &full_bar[stage], kb * 128, mt * 128);
+            bulk_load(sSFA, p.sfa + (static_cast<int64_t>(mt) * p.sf_atoms + kb * 4) * 512, ks * 512,
+                      &full_bar[stage]);
+          }
+          if constexpr (Cfg::CL == 1) {
 #pragma unroll
-          for (int j = 0; j < Cfg::NBLK; ++j) {
+            for (int j = 0; j < Cfg::NBLK; ++j) {
+              if (b_row[j] < p.b_rows_total) {
+                tma_load_2d(sB + j * 128 * 128, &tmB, &full_bar[stage], kb * 128, b_row[j]);
+                bulk_load(sSFB + j * 2048,
+                          p.sfb + (static_cast<int64_t>(b_row[j] >> 7) * p.sf_atoms + kb * 4) * 512, ks * 512,
+                          &full_bar[stage]);
+              }
+            }
+          } else {
+            // this CTA's slice of B (SLICE rows) and its share of the B scale
+            // atoms, multicast to every CTA of the cluster
+            const int j = (rank * Cfg::SLICE) / 128;
             if (b_row[j] < p.b_rows_total) {
-              tma_load_2d(sB + j * 128 * 128, &tmB, &full_bar[stage], kb * 128, b_row[j]);
-              bulk_load(sSFB + j * 2048, p.sfb + (static_cast<int64_t>(b_row[j] >> 7) * p.sf_atoms + kb * 4) * 512,
-                        ks * 512, &full_bar[stage]);
+              tma_load_2d_mc(sB + rank * Cfg::SLICE * 128, &tmB, &full_bar[stage], kb * 128,
+                             nt * BN + rank * Cfg::SLICE, kClusterMask);
+              constexpr int kRanksPerBlock = Cfg::CL / Cfg::NBLK;
+              constexpr int kAtomsPerRank = 4 / kRanksPerBlock;
+              const int a0 = (rank % kRanksPerBlock) * kAtomsPerRank;
+              const int na = min(ks, a0 + kAtomsPerRank) - a0;
+              if (na > 0)
+                bulk_load_mc(sSFB + j * 2048 + a0 * 512,
+                             p.sfb + (static_cast<int64_t>(b_row[j] >> 7) * p.sf_atoms + kb * 4 + a0) * 512,
+                             na * 512, &full_bar[stage], kClusterMask);
             }
           }
           issued[stage] = true;
@@ -251,10 +286,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // every copy this thread started lands before the CTA can exit
+      // and every release of them (from every CTA of the cluster) has arrived
       int drain_abort = 0;
 #pragma unroll
       for (int s = 0; s < STAGES; ++s)
-        if (issued[s]) mbar_wait(&full_bar[s], last_phase[s], reinterpret_cast<volatile int*>(&drain_abort), p.status);
+        if (issued[s]) {
+          mbar_wait(&full_bar[s], last_phase[s], reinterpret_cast<volatile int*>(&drain_abort), p.status);
+          mbar_wait(&empty_bar[s], last_phase[s], reinterpret_cast<volatile int*>(&drain_abort), p.status);
+        }
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
       if (lane == 0) {
@@ -268,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t kStageUnits = Cfg::STAGE_BYTES >> 4;
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        for (int tile = unit0; ok && tile < total; tile += unit_step) {
           if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1, &abort_flag, p.status)) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * BN;
@@ -289,7 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_nvfp4(d_tmem, da + 2 * s, db + 2 * s, idesc, t_sfa + 4 * s, t_sfb + (BN / 32) * s,
                            (kb > 0 || s > 0) ? 1u : 0u);
             }
-            umma_commit(&empty_bar[stage]);
+            if constexpr (Cfg::CL > 1)
+              umma_commit_mc(&empty_bar[stage], kClusterMask);
+            else
+              umma_commit(&empty_bar[stage]);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1;
@@ -319,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     uint32_t stage = 0, phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+    for (int tile = unit0; ok && tile < total; tile += unit_step) {
       for (int kb = 0; kb < p.kblocks; ++kb) {
         if (!mbar_wait(&full_bar[stage], phase, &abort_flag, p.status)) {
           ok = false;
@@ -374,8 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc = 0, acc_phase = 0;
     const float alpha_dense = (MODE == kEpiDense) ? __ldg(p.alpha) : 0.0f;
     const float g_out = (MODE == kEpiGatedQuant) ? __ldg(p.g_out) : 0.0f;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+    for (int tile = unit0; tile < total; tile += unit_step) {
+      const int mg = tile / p.n_tiles, nt = tile - mg * p.n_tiles;
+        const int mt = mg * Cfg::CL + rank;
       if (!mbar_wait(&accf_bar[acc], acc_phase, &abort_flag, p.status)) break;
       tc_fence_after();
       const int row = 32 * q + lane;
@@ -463,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (Cfg::CL > 1) cluster_sync();  // no peer arrives or writes into this CTA after this point
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
@@ -472,7 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-using DenseCfg = GemmCfg<256, 1, 4, kEpiDense>;
+using Dense1Cfg = GemmCfg<256, 1, 4, kEpiDense, 1>;
+using Dense2Cfg = GemmCfg<256, 1, 4, kEpiDense, 2>;
+using Dense4Cfg = GemmCfg<256, 1, 4, kEpiDense, 4>;
 using GatedCfg = GemmCfg<256, 1, 4, kEpiGatedQuant>;
 using AmaxCfg = GemmCfg<256, 1, 4, kEpiGatedAmax>;
 using DownCfg = GemmCfg<128, 2, 6, kEpiDownSum>;
@@ -486,13 +532,47 @@ static cudaError_t launch_cfg(const GemmMaps& maps, const GemmParams& p, int gri
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gemm_nvfp4_kernel<Cfg><<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(maps.a, maps.b, p);
+  if constexpr (Cfg::CL == 1) {
+    gemm_nvfp4_kernel<Cfg><<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(maps.a, maps.b, p);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = Cfg::CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    // the persistent grid must fit in one wave of co-resident clusters
+    static int max_clusters = -1;
+    if (max_clusters < 0) {
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(Cfg::CL, 1, 1);
+      q.blockDim = dim3(kThreads, 1, 1);
+      q.dynamicSmemBytes = Cfg::SMEM_BYTES;
+      q.attrs = attr;
+      q.numAttrs = 1;
+      int n = 0;
+      max_clusters = (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_kernel<Cfg>, &q) == cudaSuccess) ? n : 0;
+    }
+    if (max_clusters > 0 && grid / Cfg::CL > max_clusters) grid = max_clusters * Cfg::CL;
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel<Cfg>, maps.a, maps.b, p);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream,
+                        int cluster) {
   switch (mode) {
-    case kEpiDense: return launch_cfg<DenseCfg>(maps, p, grid, stream);
+    case kEpiDense:
+      if (cluster == 4) return launch_cfg<Dense4Cfg>(maps, p, grid, stream);
+      if (cluster == 2) return launch_cfg<Dense2Cfg>(maps, p, grid, stream);
+      return launch_cfg<Dense1Cfg>(maps, p, grid, stream);
     case kEpiGatedQuant: return launch_cfg<GatedCfg>(maps, p, grid, stream);
     case kEpiGatedAmax: return launch_cfg<AmaxCfg>(maps, p, grid, stream);
     case kEpiDownSum: return launch_cfg<DownCfg>(maps, p, grid, stream);
@@ -500,6 +580,5 @@ cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int
   }
 }
 
-int gemm_max_ctas_per_sm(int) { return 1; }
 
 }  // namespace nvfp4

@@ -60,11 +60,15 @@ struct GemmMaps {
   CUtensorMap b;
 };
 
-// Build a 2D TMA map over a [rows, row_bytes] byte matrix, box 128 x 128 bytes,
-// 128-byte swizzle.
-bool make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes);
+// Build a 2D TMA map over a [rows, row_bytes] byte matrix, box box_rows x 128
+// bytes, 128-byte swizzle.
+bool make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows = 128);
 
-cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream);
-int gemm_max_ctas_per_sm(int mode);
+// `cluster` (dense mode only): CTAs per cluster sharing each B tile through
+// TMA multicast (1, 2 or 4); the grid must be a multiple of it.  The B map's
+// box holds 128 rows for cluster 1 and 2 and 64 rows for cluster 4 (one box
+// per CTA and 128-row block).
+cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream,
+                        int cluster = 1);
 
 }  // namespace nvfp4
