@@ -135,8 +135,19 @@ size_t nvfp4_linear_w4a16_workspace(int64_t T, int64_t N, int64_t K);
  *   d_alpha one fp32 = 1 / g_w
  *   out     bf16 [T, N], row stride ldo >= N
  *   workspace of nvfp4_linear_w4a16_workspace(T, N, K) bytes (may be NULL when
- *   that is 0); split-K partials are summed in a fixed order, so the result is
- *   the same from run to run. */
+ *   that is 0).  The k-split partial sums of a 128-row block are summed on
+ *   chip, inside a thread-block cluster, so the query returns 0, unless the
+ *   activations of one k-split do not fit in shared memory next to the weight
+ *   (long K at large T, e.g. T = 16 with K > 24576); those shapes keep fp32
+ *   partials in the workspace and sum them with a second kernel.  Either way
+ *   the partials are summed in a fixed order, so the result is the same from
+ *   run to run.
+ * The call is launched as a programmatic dependent launch: it starts copying
+ * its weight into shared memory while the preceding kernel on the stream
+ * finishes, if that kernel allows it (this library's decode kernel does, and
+ * writes no weight); it reads x and alpha and writes out only after the
+ * preceding kernel has completed.  Back-to-back decode calls (a layer stack in
+ * a CUDA graph) overlap this way. */
 nvfp4_status nvfp4_linear_w4a16(const void* x_bf16, int64_t T, int64_t ldx,
                                 const uint8_t* w_codes, const uint8_t* w_sf, int64_t N, int64_t K,
                                 const float* d_alpha, void* out_bf16, int64_t ldo,

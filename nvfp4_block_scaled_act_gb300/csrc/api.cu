@@ -96,6 +96,20 @@ int dense_cluster(int64_t m_tiles) {
 
 }  // namespace
 
+// Codes of the decode weight: boxes of 64 bytes (one 128-k block) x 128 rows,
+// no swizzle; rows past N read as zero codes.
+bool make_gemv_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -289,6 +303,7 @@ size_t nvfp4_linear_w4a16_workspace(int64_t T, int64_t N, int64_t K) {
   if (T <= 0 || N <= 0 || K <= 0 || K % 128 != 0) return 0;
   const DeviceInfo* dev = device_info();
   const int sms = dev ? dev->sms : 152;
+  if (T <= 16 && gemv_ring_plan(T, N, K, sms).ok) return 0;  // partials stay on chip
   return gemv_plan(T, N, K, sms).ws_bytes;
 }
 
@@ -305,6 +320,13 @@ nvfp4_status nvfp4_linear_w4a16(const void* x, int64_t T, int64_t ldx, const uin
     return NVFP4_ERR_MISALIGNED;
   const DeviceInfo* dev = device_info();
   if (!dev) return NVFP4_ERR_NO_DEVICE;
+  const GemvRingPlan ring = gemv_ring_plan(T, N, K, dev->sms);
+  if (ring.ok) {
+    CUtensorMap cmap;
+    if (!make_gemv_codes_map(&cmap, w_codes, N, K / 2)) return NVFP4_ERR_CUDA;
+    return cuda_status(launch_gemv_w4a16_ring(cmap, x, T, ldx, w_sf, N, K, d_alpha, out, ldo, ring, dev->status,
+                                              stream));
+  }
   const GemvPlan plan = gemv_plan(T, N, K, dev->sms);
   if (plan.ws_bytes > 0) {
     if (!workspace) return NVFP4_ERR_INVALID_ARG;

@@ -226,6 +226,421 @@ __global__ void __launch_bounds__(256) gemv_reduce_kernel(const float* __restric
   }
 }
 
+// ---------------------------------------------------------------------------
+// Default decode path.
+//
+// A CTA owns one 128-row block of the weight and a k-range of kc elements; the
+// k-ranges of a row block form one thread-block cluster (at most 8 CTAs), and
+// the cluster sums its partials through distributed shared memory in rank
+// order, so the result is deterministic and no workspace is needed.
+//
+// Weight stream.  One producer lane copies the CTA's slice into a ring of
+// shared-memory slots: per 128-k block one TMA tile of codes (64 bytes x 128
+// rows) and its two scale atoms (1 KB, contiguous in the swizzled layout).  As
+// many slots as fit are filled before the kernel waits for the preceding
+// kernel on the stream (programmatic dependent launch), so the weight stream of
+// back-to-back decode calls overlaps the end of the previous call; the
+// producer refills slots as the compute warps release them.
+//
+// Arithmetic.  Eight compute warps: four row groups of 32 rows x two k
+// parities.  mma.sync.m16n8k16 with 16 weight rows as A and 8 tokens as B
+// (tokens 8..15 in a second MMA), fp32 accumulate.  Inside a 128-k block the
+// k order is permuted so that one 16-byte code load of row r (k = 32t .. 32t+31
+// for lane t) feeds A of that row directly; the activations are staged in the
+// same order.  A code byte becomes an f16x2 pair with one hardware conversion,
+// times the block scale: e2m1 * E4M3 has at most 6 significant bits and lies
+// in [2^-10, 2688], so it is exact in f16.  Activations are bf16; they are
+// staged as f16 after a per-token power-of-two rescale chosen from the
+// token's largest magnitude in the CTA's k-range (that magnitude lands in
+// [2^14, 2^15)): every value within 2^32 of it converts exactly, and the
+// rescale is undone exactly on the fp32 partial sums.  Products of f16 values
+// are exact in fp32.
+// ---------------------------------------------------------------------------
+constexpr int kRingRows = 128;                        // weight rows per CTA (one scale-atom row block)
+constexpr int kRingWarps = 8;                         // 4 row groups x 2 k parities
+constexpr int kRingThreads = (kRingWarps + 1) * 32;   // + one producer warp
+constexpr int kRingMaxSlots = 24;
+constexpr int kRingChunk = kRingRows * 64;            // codes of one 128-k block
+constexpr int kRingChunkSf = 1024;                    // its two scale atoms
+constexpr int kRingSlot = kRingChunk + kRingChunkSf;
+constexpr int kRingMaxCluster = 8;
+constexpr size_t kRingSmemBudget = 109 * 1024;        // two CTAs per SM with their static shared memory
+
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void e2m1x4_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two E4M3 scale bytes -> (S_lo, S_lo) and (S_hi, S_hi) as f16x2.
+__device__ __forceinline__ void scale_pair_f16(uint32_t two_bytes, uint32_t& lo, uint32_t& hi) {
+  uint32_t h2;
+  const uint16_t in = static_cast<uint16_t>(two_bytes & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  lo = __byte_perm(h2, 0, 0x1010);
+  hi = __byte_perm(h2, 0, 0x3232);
+}
+
+// Activation chunk (8 f16, 16 bytes) c of a 128-k block sits at chunk
+// c ^ (((c >> 3) & 1) << 1): with a row stride of 16 (mod 32) bytes the four
+// chunks a quarter-warp reads together fall on distinct bank groups.
+__device__ __forceinline__ int xchunk(int c) { return c ^ (((c >> 3) & 1) << 1); }
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+  return v;
+}
+
+// Power-of-two exponent that puts a token's largest magnitude (fp32 bits) in
+// [2^14, 2^15), clamped so that 2^shift and 2^-shift stay normal floats.
+__device__ __forceinline__ int token_shift(unsigned int amax_bits) {
+  const int sh = amax_bits ? static_cast<int>((amax_bits >> 23) & 0xFF) - 127 - 14 : 0;
+  return sh < -110 ? -110 : (sh > 113 ? 113 : sh);
+}
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
+
+template <bool kTok16>
+__global__ void __launch_bounds__(kRingThreads) gemv_ring_kernel(
+    const __grid_constant__ CUtensorMap cmap, const uint16_t* __restrict__ x, int T, int64_t ldx,
+    const uint8_t* __restrict__ w_sf, int N, int K, int kc, int R, const float* __restrict__ d_alpha,
+    uint16_t* __restrict__ out, int64_t ldo, int* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  __shared__ unsigned int tok_amax[16];
+  __shared__ __align__(8) uint64_t full[kRingMaxSlots];
+  __shared__ __align__(8) uint64_t empty[kRingMaxSlots];
+  __shared__ volatile int abort_flag;
+  pdl_launch_dependents();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool producer = (warp == kRingWarps) && lane == 0;
+  if (producer) prefetch_tmap(&cmap);
+  const uint32_t ncl = cluster_nctarank();
+  const uint32_t rank = cluster_ctarank();
+  const int rb = static_cast<int>(blockIdx.x / ncl);
+  const int k_begin = static_cast<int>(rank) * kc;
+  const int k_len = max(0, min(kc, K - k_begin));
+  const int nkb = k_len / 128;
+  uint8_t* ring = sm;                                             // R x codes
+  uint8_t* ring_sf = ring + R * kRingChunk;                       // R x scales
+  const int xs_stride = kc * 2 + 16;
+  uint8_t* xs = ring_sf + R * kRingChunkSf;                       // [T][kc*2+16] f16 activations
+  float* part = reinterpret_cast<float*>(xs + T * xs_stride);     // [2][T][128] partial sums
+  const uint8_t* sf_src = w_sf + (static_cast<int64_t>(rb) * (K / 64) + k_begin / 64) * 512;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < R; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 4);
+    }
+    fence_barrier_init();
+  }
+  if (threadIdx.x < 16) tok_amax[threadIdx.x] = 0u;
+  __syncthreads();
+  int issued = 0;  // producer: fills issued so far (chunk c goes to slot c % R, phase c / R)
+  if (producer) {
+    // the weight does not depend on the preceding kernel: fill the ring now
+    const int pre = min(R, nkb);
+    issued = pre;
+    for (int c = 0; c < pre; ++c) {
+      mbar_arrive_expect_tx(&full[c], kRingSlot);
+      tma_load_2d(ring + c * kRingChunk, &cmap, &full[c], k_begin / 2 + c * 64, rb * kRingRows);
+      bulk_load(ring_sf + c * kRingChunkSf, sf_src + c * kRingChunkSf, kRingChunkSf, &full[c]);
+    }
+  }
+
+  // activations, alpha and the output follow the preceding kernel
+  pdl_wait();
+  const float alpha = __ldg(d_alpha);
+  const int units = k_len / 8;  // 16-byte activation units per token (a multiple of 16)
+  constexpr int kComp = kRingWarps * 32;
+  if (warp < kRingWarps) {
+    constexpr int kXB = 4;
+    for (int u0 = threadIdx.x; u0 - static_cast<int>(threadIdx.x) < T * units; u0 += kXB * kComp) {
+      uint4 v[kXB];
+#pragma unroll
+      for (int q = 0; q < kXB; ++q) {
+        const int u = u0 + q * kComp;
+        v[q] = make_uint4(0u, 0u, 0u, 0u);
+        if (u < T * units) {
+          const int tok = u / units;
+          v[q] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * ldx + k_begin +
+                                                      (u - tok * units) * 8));
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kXB; ++q) {
+        const int ubase = u0 + q * kComp - lane;  // first unit of this warp (warp-uniform)
+        if (ubase >= T * units) break;
+        const int u = ubase + lane;
+        const bool in = u < T * units;
+        const int tok = in ? u / units : T;
+        const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+        float m = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          m = fmaxf(m, fabsf(bf16_bits_to_f32(w4[e] & 0xFFFFu)));
+          m = fmaxf(m, fabsf(bf16_bits_to_f32(w4[e] >> 16)));
+        }
+        // the 32 units of a warp span at most three tokens
+        const int t0 = ubase / units, t1 = min(T - 1, (ubase + 31) / units);
+        for (int tt = t0; tt <= t1; ++tt) {
+          const unsigned int mb = __reduce_max_sync(0xFFFFFFFFu, (in && tok == tt) ? __float_as_uint(m) : 0u);
+          if (lane == 0 && mb != 0u) atomicMax(&tok_amax[tt], mb);
+        }
+        if (in) {
+          const int k8 = (u - tok * units) * 8;
+          *reinterpret_cast<uint4*>(xs + tok * xs_stride + (k8 >> 7) * 256 + xchunk((k8 & 127) >> 3) * 16) = v[q];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp < kRingWarps) {
+    // in place: bf16 -> f16 after the token's power-of-two rescale
+    for (int u = threadIdx.x; u < T * units; u += kComp) {
+      const int tok = u / units;
+      const float f = pow2f(-token_shift(tok_amax[tok]));
+      const int k8 = (u - tok * units) * 8;
+      uint4* slot = reinterpret_cast<uint4*>(xs + tok * xs_stride + (k8 >> 7) * 256 + xchunk((k8 & 127) >> 3) * 16);
+      const uint4 v = *slot;
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __half2 h = __floats2half2_rn(bf16_bits_to_f32(w4[e] & 0xFFFFu) * f, bf16_bits_to_f32(w4[e] >> 16) * f);
+        o[e] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *slot = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  __syncthreads();
+
+  if (producer) {
+    // refill slots as the compute warps release them (after the barriers above,
+    // which the compute warps pass before they consume anything)
+    int s = 0, round = 1;
+    for (int c = R; c < nkb; ++c) {
+      if (!mbar_wait(&empty[s], (round - 1) & 1, &abort_flag, status)) break;
+      mbar_arrive_expect_tx(&full[s], kRingSlot);
+      tma_load_2d(ring + s * kRingChunk, &cmap, &full[s], k_begin / 2 + c * 64, rb * kRingRows);
+      bulk_load(ring_sf + s * kRingChunkSf, sf_src + c * kRingChunkSf, kRingChunkSf, &full[s]);
+      ++issued;
+      if (++s == R) {
+        s = 0;
+        ++round;
+      }
+    }
+  } else if (warp < kRingWarps) {
+    const int g = lane >> 2, t = lane & 3;
+    const int kp = warp >> 2;
+    const int lr0 = (warp & 3) * 32;
+    int sf_off[4], cofs[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int lr = lr0 + 8 * j + g;
+      sf_off[j] = (lr & 31) * 16 + (lr >> 5) * 4 + 2 * (t & 1) + (t >> 1) * 512;
+      cofs[j] = lr * 64 + 16 * t;
+    }
+    int xofs[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) xofs[i] = g * xs_stride + xchunk(4 * t + i) * 16;
+    const bool tok_lo = g < T, tok_hi = g + 8 < T;
+    // acc[a][h][c]: rows lr0 + 16a + g (+8 for c >= 2) x tokens 8h + 2t (+1 for odd c)
+    float acc[2][kTok16 ? 2 : 1][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int h = 0; h < (kTok16 ? 2 : 1); ++h)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[a][h][c] = 0.0f;
+    int s = kp, round = 0;
+    while (s >= R) {
+      s -= R;
+      ++round;
+    }
+    for (int kb = kp; kb < nkb; kb += 2) {
+      if (!mbar_wait(&full[s], round & 1, &abort_flag, status)) break;
+      const uint8_t* cs = ring + s * kRingChunk;
+      const uint8_t* ss = ring_sf + s * kRingChunkSf;
+      uint4 cw[4];
+      uint32_t slo[4], shi[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        cw[j] = *reinterpret_cast<const uint4*>(cs + cofs[j]);
+        scale_pair_f16(*reinterpret_cast<const uint16_t*>(ss + sf_off[j]), slo[j], shi[j]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      s += 2;
+      while (s >= R) {
+        s -= R;
+        ++round;
+      }
+      const uint8_t* xb = xs + kb * 256;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint4 blo = make_uint4(0u, 0u, 0u, 0u), bhi = make_uint4(0u, 0u, 0u, 0u);
+        if (tok_lo) blo = *reinterpret_cast<const uint4*>(xb + xofs[i]);
+        if (kTok16 && tok_hi) bhi = *reinterpret_cast<const uint4*>(xb + xofs[i] + 8 * xs_stride);
+        uint32_t wf[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t word = (i == 0) ? cw[j].x : (i == 1) ? cw[j].y : (i == 2) ? cw[j].z : cw[j].w;
+          const uint32_t m = (i < 2) ? slo[j] : shi[j];
+          e2m1x4_to_f16x2(word, wf[j]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) wf[j][e] = f16x2_mul(wf[j][e], m);
+        }
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          // A: rows g / g+8 of tile a, k pairs (0,1) then (2,3) of code word i
+          mma_f16_16816(acc[a][0], wf[2 * a][0], wf[2 * a + 1][0], wf[2 * a][1], wf[2 * a + 1][1], blo.x, blo.y);
+          mma_f16_16816(acc[a][0], wf[2 * a][2], wf[2 * a + 1][2], wf[2 * a][3], wf[2 * a + 1][3], blo.z, blo.w);
+          if (kTok16) {
+            mma_f16_16816(acc[a][kTok16 ? 1 : 0], wf[2 * a][0], wf[2 * a + 1][0], wf[2 * a][1], wf[2 * a + 1][1],
+                          bhi.x, bhi.y);
+            mma_f16_16816(acc[a][kTok16 ? 1 : 0], wf[2 * a][2], wf[2 * a + 1][2], wf[2 * a][3], wf[2 * a + 1][3],
+                          bhi.z, bhi.w);
+          }
+        }
+      }
+    }
+    // partials with the rescale undone -> part[kp][tok][row]
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int h = 0; h < (kTok16 ? 2 : 1); ++h)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int row = lr0 + a * 16 + g + 8 * (c >> 1);
+          const int tok = h * 8 + 2 * t + (c & 1);
+          if (tok < T) part[(kp * T + tok) * kRingRows + row] = acc[a][h][c] * pow2f(token_shift(tok_amax[tok]));
+        }
+  }
+  __syncthreads();
+  if (abort_flag && producer) {
+    // wind down after a timed-out wait: let this CTA's copies still in flight
+    // land (bounded) before its shared memory is released
+    const long long t0 = clock64();
+    for (int i = 0; i < R && i < issued; ++i) {
+      const int last = i + ((issued - 1 - i) / R) * R;  // last chunk issued into slot i
+      while (!mbar_try_wait(smem_u32(&full[i]), (last / R) & 1) && clock64() - t0 < kWaitLimitCycles) {
+      }
+    }
+  }
+  // rank r sums rows [r * rows_per, ...) of the cluster's partials in rank order
+  cluster_arrive();
+  cluster_wait();
+  const int rows_per = (kRingRows + static_cast<int>(ncl) - 1) / static_cast<int>(ncl);
+  for (int e = threadIdx.x; e < T * rows_per; e += blockDim.x) {
+    const int tok = e / rows_per;
+    const int row = static_cast<int>(rank) * rows_per + (e - tok * rows_per);
+    if (row >= kRingRows) continue;
+    float v[2 * kRingMaxCluster];
+#pragma unroll
+    for (int q = 0; q < kRingMaxCluster; ++q) {
+      v[2 * q] = q < static_cast<int>(ncl) ? ld_cluster_f32(part + tok * kRingRows + row, q) : 0.0f;
+      v[2 * q + 1] = q < static_cast<int>(ncl) ? ld_cluster_f32(part + (T + tok) * kRingRows + row, q) : 0.0f;
+    }
+    float sum = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 2 * kRingMaxCluster; ++q) sum += v[q];
+    const int n = rb * kRingRows + row;
+    if (n < N) out[static_cast<int64_t>(tok) * ldo + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum * alpha));
+  }
+  cluster_arrive();
+  cluster_wait();
+}
+
+GemvRingPlan gemv_ring_plan(int64_t T, int64_t N, int64_t K, int num_sms) {
+  GemvRingPlan p{};
+  const int64_t row_blocks = (N + kRingRows - 1) / kRingRows;
+  const int64_t kblocks = K / 128;
+  int64_t cl = (2 * static_cast<int64_t>(num_sms)) / row_blocks;
+  cl = cl < 1 ? 1 : (cl > kRingMaxCluster ? kRingMaxCluster : cl);
+  if (cl > kblocks) cl = kblocks;
+  const int64_t kcb = (kblocks + cl - 1) / cl;
+  p.cl = static_cast<int>(cl);
+  p.kc = static_cast<int>(kcb * 128);
+  p.row_blocks = row_blocks;
+  const size_t fixed = static_cast<size_t>(T) * (kcb * 256 + 16) + static_cast<size_t>(2 * T * kRingRows * 4);
+  int64_t slots = fixed < kRingSmemBudget ? static_cast<int64_t>((kRingSmemBudget - fixed) / kRingSlot) : 0;
+  if (slots > kcb) slots = kcb;
+  if (slots > kRingMaxSlots) slots = kRingMaxSlots;
+  p.R = static_cast<int>(slots);
+  p.ok = slots >= 2 || (slots >= 1 && kcb == 1);
+  p.smem = fixed + static_cast<size_t>(slots) * kRingSlot + 1024;  // + alignment slack
+  return p;
+}
+
+template <bool kTok16>
+static cudaError_t launch_ring_t(const CUtensorMap& cmap, const void* x, int64_t T, int64_t ldx, const uint8_t* w_sf,
+                                 int64_t N, int64_t K, const float* d_alpha, void* out, int64_t ldo,
+                                 const GemvRingPlan& plan, int* status, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_ring_kernel<kTok16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kRingSmemBudget + 1024));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(plan.row_blocks * plan.cl));
+  cfg.blockDim = dim3(kRingThreads);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(plan.cl);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemv_ring_kernel<kTok16>, cmap, static_cast<const uint16_t*>(x),
+                            static_cast<int>(T), ldx, w_sf, static_cast<int>(N), static_cast<int>(K), plan.kc, plan.R,
+                            d_alpha, static_cast<uint16_t*>(out), ldo, status);
+}
+
+cudaError_t launch_gemv_w4a16_ring(const CUtensorMap& cmap, const void* x, int64_t T, int64_t ldx,
+                                   const uint8_t* w_sf, int64_t N, int64_t K, const float* d_alpha, void* out,
+                                   int64_t ldo, const GemvRingPlan& plan, int* status, cudaStream_t stream) {
+  if (T > 8) return launch_ring_t<true>(cmap, x, T, ldx, w_sf, N, K, d_alpha, out, ldo, plan, status, stream);
+  return launch_ring_t<false>(cmap, x, T, ldx, w_sf, N, K, d_alpha, out, ldo, plan, status, stream);
+}
+
 GemvPlan gemv_plan(int64_t T, int64_t N, int64_t K, int num_sms) {
   GemvPlan p;
   p.row_blocks = static_cast<int>((N + kGemvRows - 1) / kGemvRows);

@@ -1,6 +1,7 @@
 // MoE workspace carving and launchers (moe.cu), shared with api.cu.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -53,5 +54,20 @@ GemvPlan gemv_plan(int64_t T, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_gemv_w4a16(const void* x, int64_t T, int64_t ldx, const uint8_t* w_codes, const uint8_t* w_sf,
                               int64_t N, int64_t K, const float* d_alpha, void* out, int64_t ldo, float* ws,
                               const GemvPlan& plan, cudaStream_t stream);
+
+// Default decode path: weight ring in shared memory, split-K inside a
+// thread-block cluster, programmatic dependent launch; no workspace.
+struct GemvRingPlan {
+  int cl;              // CTAs per cluster (k-splits of a row block)
+  int kc;              // k elements per CTA
+  int R;               // ring slots (128-k blocks resident at once)
+  int64_t row_blocks;  // ceil(N / 128)
+  size_t smem;         // dynamic shared memory per CTA
+  bool ok;             // false: the activations of a CTA do not fit; use the split-K path
+};
+GemvRingPlan gemv_ring_plan(int64_t T, int64_t N, int64_t K, int num_sms);
+cudaError_t launch_gemv_w4a16_ring(const CUtensorMap& cmap, const void* x, int64_t T, int64_t ldx,
+                                   const uint8_t* w_sf, int64_t N, int64_t K, const float* d_alpha, void* out,
+                                   int64_t ldo, const GemvRingPlan& plan, int* status, cudaStream_t stream);
 
 }  // namespace nvfp4

@@ -13,6 +13,8 @@
 
 namespace nvfp4 {
 
+constexpr int kQuantUnroll = 4;  // chunks per warp, loads issued together
+
 __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                         int64_t ldx, const float* __restrict__ d_global,
                                                         uint8_t* __restrict__ codes,
@@ -21,20 +23,30 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restri
   const float g = __ldg(d_global);
   const int lane = threadIdx.x & 31;
   const int64_t chunks = (Cp * 16 + 255) / 256;  // per row, padded columns included
+  const int64_t total = Mp * chunks;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int64_t cpad4 = Cp / 4;
-  for (int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; item < Mp * chunks;
-       item += nwarps) {
-    const int64_t r = item / chunks;
-    const int64_t ch = item - r * chunks;
-    const int64_t c = ch * 16 + (lane >> 1);
-    const int64_t k0 = ch * 256 + lane * 8;
-    const bool real = (r < M) && (c < C);
-    float v[8];
-    float amax = 0.0f;
-    if (real) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(x + r * ldx + k0));
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  for (int64_t base = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * kQuantUnroll;
+       base < total; base += nwarps * kQuantUnroll) {
+    uint4 raw[kQuantUnroll];
+    int64_t rr[kQuantUnroll], cc[kQuantUnroll], kk[kQuantUnroll];
+    bool real[kQuantUnroll];
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const int64_t item = base + u;
+      const int64_t r = item / chunks;
+      const int64_t ch = item - r * chunks;
+      rr[u] = r;
+      cc[u] = ch * 16 + (lane >> 1);
+      kk[u] = ch * 256 + lane * 8;
+      real[u] = (item < total) && (r < M) && (cc[u] < C);
+      raw[u] = real[u] ? __ldg(reinterpret_cast<const uint4*>(x + r * ldx + kk[u])) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+      float v[8];
+      float amax = 0.0f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         v[2 * j] = bf16_bits_to_f32(w[j] & 0xFFFFu);
@@ -42,22 +54,20 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restri
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
-    } else {
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      const BlockScale bs = block_scale(amax, g);
+      if (real[u]) {
+        uint32_t packed = 0;
+        if (bs.r != 0.0f) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
-    }
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-    const BlockScale bs = block_scale(amax, g);
-    if (real) {
-      uint32_t packed = 0;
-      if (bs.r != 0.0f) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          packed |= f32x2_to_e2m1x2(__fmul_rn(v[2 * j], bs.r), __fmul_rn(v[2 * j + 1], bs.r)) << (8 * j);
+          for (int j = 0; j < 4; ++j)
+            packed |= f32x2_to_e2m1x2(__fmul_rn(v[2 * j], bs.r), __fmul_rn(v[2 * j + 1], bs.r)) << (8 * j);
+        }
+        *reinterpret_cast<uint32_t*>(codes + rr[u] * (K / 2) + kk[u] / 2) = packed;
       }
-      *reinterpret_cast<uint32_t*>(codes + r * (K / 2) + k0 / 2) = packed;
+      if ((lane & 1) == 0 && base + u < total && rr[u] < Mp && cc[u] < Cp)
+        scales[sf_offset(rr[u], cc[u], cpad4)] = real[u] ? static_cast<uint8_t>(bs.s8) : 0;
     }
-    if ((lane & 1) == 0 && c < Cp) scales[sf_offset(r, c, cpad4)] = real ? static_cast<uint8_t>(bs.s8) : 0;
   }
 }
 
@@ -130,7 +140,7 @@ cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, c
                              uint8_t* codes, uint8_t* scales, cudaStream_t stream) {
   const int64_t C = K / 16, Cp = (C + 3) / 4 * 4, Mp = (M + 127) / 128 * 128;
   const int64_t items = Mp * ((Cp * 16 + 255) / 256);
-  const int64_t want = (items + 7) / 8;
+  const int64_t want = (items + 8 * kQuantUnroll - 1) / (8 * kQuantUnroll);
   const int blocks = static_cast<int>(want < 1 ? 1 : (want > 65535 ? 65535 : want));
   quant_act_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), M, K, ldx, d_global, codes, scales,
                                                Mp, C, Cp);

@@ -127,8 +127,13 @@ def test_w4a16_decode_shapes(nv, T, N, K):
 
 
 @pytest.mark.parametrize("T,N,K", [(1, 8, 128), (3, 136, 384), (5, 1032, 256), (7, 264, 640),
-                                   (9, 520, 128), (15, 2056, 1152), (16, 16, 4096), (2, 3584, 5120)])
+                                   (9, 520, 128), (15, 2056, 1152), (16, 16, 4096), (2, 3584, 5120),
+                                   (1, 256, 32768), (16, 256, 32768)])
 def test_w4a16_ragged(nv, T, N, K):
+    """Ragged N (partial 128-row blocks), T across both token layouts, and long
+    K: (1, 256, 32768) streams more 128-k blocks than the shared-memory ring
+    holds, (16, 256, 32768) has more activations per CTA than fit next to the
+    ring and runs the split-K kernel with its workspace."""
     L = Linear(nv, synthdata.decode_case(T, N, K, seed=N + T), quant_act=False)
     out = nv.nvfp4_linear_w4a16(L.x_dev, L.W.codes, L.W.scales, L.alpha16_dev, N, K)
     check_close(out, oracle.linear_w4a16(L.x, L.wc, L.ws, N, K, L.alpha16), f"W4A16 {T}x{N}x{K}")
@@ -161,3 +166,24 @@ def test_w4a16_refuses_more_than_16_tokens(nv):
     L = Linear(nv, synthdata.decode_case(17, 64, 128, seed=1), quant_act=False)
     with pytest.raises(nv.NVFP4Error):
         nv.nvfp4_linear_w4a16(L.x_dev, L.W.codes, L.W.scales, L.alpha16_dev, 64, 128)
+
+
+@pytest.mark.parametrize("M", [8, 300, 2048])
+def test_w4a4_agrees_with_library_nvfp4_gemm(nv, M):
+    """Cross-check against cuBLASLt's NVFP4 GEMM (torch._scaled_mm on e2m1 codes
+    with E4M3 block scales in the 128x4 layout), when this torch has it: it
+    reads the same codes and scale buffers, so agreement pins the nibble order
+    and the scale layout against outside code.  The library rounds its fp32
+    sum to bf16 before alpha is applied, so the tolerance allows one more
+    bf16 rounding."""
+    L = Linear(nv, synthdata.linear_case(M, [512, 256], 1024, seed=M))
+    out = L.w4a4(nv).float()
+    try:
+        ref = torch._scaled_mm(L.ac_dev.view(torch.float4_e2m1fn_x2),
+                               L.W.codes.view(torch.float4_e2m1fn_x2).t(),
+                               L.as_dev.view(torch.float8_e4m3fn), L.W.scales.view(torch.float8_e4m3fn),
+                               out_dtype=torch.bfloat16)
+    except Exception as e:  # noqa: BLE001
+        pytest.skip(f"no NVFP4 _scaled_mm in this torch: {type(e).__name__}")
+    ref = ref.float() * L.alpha_dev.item()
+    check_close(out, ref, f"vs library NVFP4 GEMM M={M}", ulps=3.0, rel_l2=5e-3)

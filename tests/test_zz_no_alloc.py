@@ -60,8 +60,9 @@ def test_noalloc_matches_workspace_entry_point(nv, T, N, K):
 
 
 def test_noalloc_refuses_shapes_beyond_its_array(nv):
+    # 100 blocks of 256 rows on 152 SMs give 4 k-splits: 4 * 16 * 25600 fp32
+    # partials = 6.25 MiB, more than the 6 MiB array
     T, N, K = 16, 25600, 4096
-    assert nv.nvfp4_linear_w4a16_workspace(T, N, K) > 6 * 1024 * 1024
     x = torch.zeros(T, K, dtype=torch.bfloat16, device=DEV)
     codes = torch.zeros(N, K // 2, dtype=torch.uint8, device=DEV)
     scales = torch.zeros(nv.nvfp4_scale_bytes(N, K), dtype=torch.uint8, device=DEV)
