@@ -222,6 +222,22 @@ class Workload:
         return 2 + sum(d["ncopy"] * d["launches"] for d in self.decode) + 7
 
 
+def _profile_traffic(name: str):
+    """DRAM bytes per launch recorded in profiles/<name> by an ncu capture, or
+    None when the kernel source has changed since (its git blob hash differs
+    from the one recorded with the capture) or the summary is missing."""
+    import hashlib
+    try:
+        text = open(os.path.join(ROOT, "profiles", name)).read()
+        src, blob = next(l.split()[1:3] for l in text.splitlines() if l.startswith("source-blob:"))
+        nbytes = next(int(l.split()[1]) for l in text.splitlines() if l.startswith("dram-bytes-per-launch:"))
+        data = open(os.path.join(ROOT, src), "rb").read()
+        now = hashlib.sha1(b"blob %d\0" % len(data) + data).hexdigest()
+        return nbytes if now == blob else None
+    except (OSError, StopIteration, ValueError, IndexError):
+        return None
+
+
 def _timed(fn, stream):
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
@@ -296,6 +312,9 @@ def run_ours(args, world, rank, local):
         decode[f"T{d['T']}_{d['N']}x{d['K']}"] = {
             "us": round(t * 1e6, 3), "gbs": round(d["bytes"] / t / 1e9, 1),
             "frac_hbm": round(d["bytes"] / t / 1e9 / hbm, 4)}
+    head_key = f"T1_{synthdata.DECODE_SHAPES[0][0]}x{synthdata.DECODE_SHAPES[0][1]}"
+    head = decode[head_key]
+    head_bytes = next(d["bytes"] for d in wl.decode if d["T"] == 1 and (d["N"], d["K"]) == synthdata.DECODE_SHAPES[0])
     value = world * wl.pre_flops / t_pre / 1e12
     gemm_tflops = wl.pre_flops / t_gemm / 1e12
     result = {
@@ -315,11 +334,21 @@ def run_ours(args, world, rank, local):
         "decode": decode,
         "moe": {"ms": round(t_moe * 1e3, 4), "tflops": round(wl.moe_flops / t_moe / 1e12, 1),
                 "frac_fp4_peak": round(wl.moe_flops / t_moe / 1e12 / fp4_peak, 4)},
-        "roofline": {"kernel": "gemm_nvfp4_kernel (W4A4, M=8192)", "bound": "tensor",
-                     "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / fp4_peak, 4),
-                     "peak_source": f"{peak_src} bf16 burst {bf16} TFLOP/s x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
-                     "algorithmic_bytes": wl.pre_bytes, "traffic": None},
+        # the dominant kernel of the step (about 95 % of its device time, see
+        # profiles/launches_bench_step.md) is the decode GEMM; its roofline is
+        # given for the headline decode call, T = 1 on 8704 x 5120
+        "roofline": {"kernel": "gemv_ring_kernel<0> (W4A16 decode, T=1, 8704x5120)", "bound": "hbm",
+                     "achieved": round(head["gbs"], 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(head["gbs"] / hbm, 4),
+                     "peak_source": f"{peak_src} copy bandwidth",
+                     "algorithmic_bytes_per_launch": head_bytes, "launch_us": round(head["us"], 3),
+                     "traffic": _profile_traffic("gemv_w4a16_T1_8704x5120.md")},
+        "roofline_gemm": {"kernel": "gemm_nvfp4_kernel (W4A4, M=8192)", "bound": "tensor",
+                          "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                          "frac": round(gemm_tflops / fp4_peak, 4),
+                          "peak_source": f"{peak_src} bf16 burst {bf16} TFLOP/s x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
+                          "algorithmic_bytes": wl.pre_bytes,
+                          "traffic": _profile_traffic("gemm_w4a4_M8192_N7168_K5120.md")},
         "gpu_launches": wl.launches_per_step() * args.steps,
         "wall_s_timed_region": round(wall, 3),
     }
@@ -439,6 +468,57 @@ def run_reference(args, world, rank):
     }))
 
 
+def run_profile(stage: str, reps: int):
+    """One stage of the path launched `reps` times, without graphs or timing,
+    on inputs larger than the L2: the small case that the ncu summaries under
+    profiles/ are captured on."""
+    import nvfp4_block_scaled_act_gb300 as nv
+    from nvfp4_block_scaled_act_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if stage in ("gemm", "quant"):
+        pc = synthdata.prefill_case(PREFILL_M, seed=0, device=dev)
+        W = nv.quantize_weight(pc.w_parts)
+        g = nv.nvfp4_compute_global(pc.x_calib)
+        alpha = nv.nvfp4_make_alpha(g, W.g)
+        codes, sf = nv.nvfp4_quantize_act(pc.x, g)
+        out = torch.empty(PREFILL_M, W.N, dtype=torch.bfloat16, device=dev)
+        for _ in range(reps):
+            if stage == "quant":
+                nv.nvfp4_quantize_act(pc.x, g, codes, sf)
+            else:
+                nv.nvfp4_linear_w4a4(codes, sf, W.codes, W.scales, alpha, W.N, W.K, out=out)
+    elif stage == "gemv":
+        N, K = synthdata.DECODE_SHAPES[0]
+        d = synthdata.decode_case(1, N, K, seed=1, device=dev)
+        W = nv.quantize_weight(d.w_parts)
+        alpha = nv.nvfp4_make_alpha(None, W.g)
+        copies = [(W.codes, W.scales)] + [(W.codes.clone(), W.scales.clone()) for _ in range(7)]  # 8 x 25 MB
+        out = torch.empty(1, N, dtype=torch.bfloat16, device=dev)
+        for i in range(reps):
+            c, sc = copies[i % len(copies)]
+            nv.nvfp4_linear_w4a16(d.x, c, sc, alpha, N, K, out=out)
+    elif stage == "moe":
+        cfg = synthdata.MOE_SMALL
+        E, H, I, topk = cfg["E"], cfg["H"], cfg["I"], cfg["topk"]
+        mc = synthdata.moe_case(MOE_T, E, H, I, topk, cfg["skewed"], seed=0, device=dev)
+        Wm = nv.quantize_moe_weights(lambda e: mc.w13(e), lambda e: mc.w2(e), E, H, I, dev)
+        g1 = nv.nvfp4_compute_global(mc.x_calib)
+        a13 = nv.nvfp4_make_alpha(g1, Wm.g13)
+        g2, _ = nv.nvfp4_moe_calibrate(mc.x_calib, g1, Wm.w13_codes, Wm.w13_sf, a13, E, I)
+        a2 = nv.nvfp4_make_alpha(g2, Wm.g2)
+        out = torch.empty(MOE_T, H, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(nv.nvfp4_moe_workspace(MOE_T, H, I, E, topk), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            nv.nvfp4_moe_w4a4(mc.x, mc.topk_ids, mc.topk_w, g1, Wm.w13_codes, Wm.w13_sf, a13, g2, Wm.w2_codes,
+                              Wm.w2_sf, a2, E, I, out=out, workspace=ws)
+    else:
+        raise SystemExit(f"unknown stage {stage}")
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": stage, "reps": reps, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -447,8 +527,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["gemm", "quant", "gemv", "moe"],
+                    help="launch one stage a few times on a small case (for ncu), print nothing else")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
     world, rank, local = _dist()
+    if args.profile:
+        run_profile(args.profile, args.reps)
+        return
     if args.impl == "reference":
         run_reference(args, world, rank)
     else:
