@@ -16,17 +16,22 @@
 // section "Changes") were written for mma.sync on sm_120; this kernel keeps
 // their dataflow and epilogue fusion and maps it onto tcgen05 and TMEM.
 //
-// Structure (one CTA per SM, persistent over tiles n-fastest):
+// Structure (one CTA of 16 warps per SM, persistent over tiles n-fastest):
 //   warp 0      TMA producer: a 128x128-byte A box, BN/128 B boxes (128-byte
 //               swizzle) and the matching 512-byte scale atoms (bulk copies,
 //               contiguous in the 128x4 layout) into a STAGES-deep smem ring.
-//   warp 1      allocates TMEM; one lane copies each stage's scale atoms
-//               smem -> TMEM (tcgen05.cp 32x128b.warpx4) and issues 4 MMAs of
-//               K = 64 per 256-k stage; tcgen05.commit releases smem stages and
-//               publishes finished accumulators.
-//   warps 2..   epilogue: tcgen05.ld of the accumulator, fused epilogue math,
+//   warp 1      allocates TMEM; one lane issues 4 MMAs of K = 64 per 256-k
+//               stage once the stage's scales are in TMEM; tcgen05.commit
+//               releases smem stages and publishes finished accumulators.
+//   warps 4-7   scale writers: warp q copies the stage's scale atoms from smem
+//               into TMEM lane quadrant q with tcgen05.st (the replicated
+//               layout the block-scaled MMA reads), so the MMA lane issues
+//               nothing but MMAs.
+//   warps 8-15  epilogue: tcgen05.ld of the accumulator, fused epilogue math,
 //               global stores; an accumulator is released as soon as it has
 //               been read, so the next tile's MMAs overlap the epilogue math.
+// setmaxnreg moves registers from the producer/MMA/scale warps (64) to the
+// epilogue warps (192).
 // Every mbarrier wait is bounded; a timeout sets the device status word and
 // every role winds down (waiting for its own copies and MMAs) before TMEM is freed.
 #include "nvfp4_common.cuh"
