@@ -180,6 +180,9 @@ class Workload:
         nv.nvfp4_linear_w4a4(self.pre_codes, self.pre_sf, self.pre_W.codes, self.pre_W.scales, self.pre_alpha,
                              self.pre_W.N, self.pre_W.K, out=self.pre_out)
 
+    def quant_only(self):
+        self.nv.nvfp4_quantize_act(self.pre_x, self.pre_g, self.pre_codes, self.pre_sf)
+
     def gemm_only(self):
         self.nv.nvfp4_linear_w4a4(self.pre_codes, self.pre_sf, self.pre_W.codes, self.pre_W.scales,
                                   self.pre_alpha, self.pre_W.N, self.pre_W.K, out=self.pre_out)
@@ -219,7 +222,7 @@ class Workload:
         self.flush_buf.fill_(1)
 
     def launches_per_step(self) -> int:
-        return 2 + sum(d["ncopy"] * d["launches"] for d in self.decode) + 7
+        return 3 + sum(d["ncopy"] * d["launches"] for d in self.decode) + 7
 
 
 def _profile_traffic(name: str):
@@ -265,6 +268,8 @@ def run_ours(args, world, rank, local):
         ev_pre = _timed(wl.prefill, stream)
         wl.flush()
         ev_gemm = _timed(wl.gemm_only, stream)
+        wl.flush()
+        ev_quant = _timed(wl.quant_only, stream)
         dec = []
         for d in wl.decode:
             wl.flush()
@@ -272,7 +277,7 @@ def run_ours(args, world, rank, local):
         wl.flush()
         ev_moe = _timed(wl.moe, stream)
         if record is not None:
-            record.append((ev_pre, ev_gemm, dec, ev_moe))
+            record.append((ev_pre, ev_gemm, dec, ev_moe, ev_quant))
 
     for _ in range(args.warmup):
         step(None)
@@ -299,6 +304,7 @@ def run_ours(args, world, rank, local):
     t_pre = statistics.median(pre_ms) * 1e-3
     t_gemm = statistics.median(gemm_ms) * 1e-3
     t_moe = statistics.median(moe_ms) * 1e-3
+    t_quant = statistics.median([ms(r[4]) for r in recs]) * 1e-3
     per_step = sum(step_ms) / len(step_ms)
     if world > 1:
         t = torch.tensor([t_pre, per_step], device=dev)
@@ -331,6 +337,8 @@ def run_ours(args, world, rank, local):
                     "frac_fp4_peak": round(wl.pre_flops / t_pre / 1e12 / fp4_peak, 4)},
         "gemm_w4a4": {"ms": round(t_gemm * 1e3, 4), "tflops": round(gemm_tflops, 1),
                       "frac_fp4_peak": round(gemm_tflops / fp4_peak, 4)},
+        "quant_act": {"us": round(t_quant * 1e6, 2), "gbs": round(wl.quant_bytes / t_quant / 1e9, 1),
+                      "frac_hbm": round(wl.quant_bytes / t_quant / 1e9 / hbm, 4)},
         "decode": decode,
         "moe": {"ms": round(t_moe * 1e3, 4), "tflops": round(wl.moe_flops / t_moe / 1e12, 1),
                 "frac_fp4_peak": round(wl.moe_flops / t_moe / 1e12 / fp4_peak, 4)},

@@ -257,8 +257,9 @@ nvfp4_status nvfp4_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx
   if (!x || !d_global || !codes || !scales) return NVFP4_ERR_INVALID_ARG;
   if (K % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || (ldx % 8) != 0) return NVFP4_ERR_MISALIGNED;
-  if (!device_info()) return NVFP4_ERR_NO_DEVICE;
-  return cuda_status(launch_quant_act(x, M, K, ldx, d_global, codes, scales, stream));
+  const DeviceInfo* dev = device_info();
+  if (!dev) return NVFP4_ERR_NO_DEVICE;
+  return cuda_status(launch_quant_act(x, M, K, ldx, d_global, codes, scales, dev->sms, stream));
 }
 
 nvfp4_status nvfp4_linear_w4a4(const uint8_t* a_codes, const uint8_t* a_sf, int64_t M, const uint8_t* w_codes,

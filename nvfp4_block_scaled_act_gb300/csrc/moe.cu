@@ -135,12 +135,13 @@ __global__ void __launch_bounds__(256) moe_quant_permute_kernel(const uint16_t* 
                                                                 float* __restrict__ y) {
   const float g = __ldg(d_g);
   const int lane = threadIdx.x & 31;
-  const int64_t chunks = (H + 255) / 256;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; item < T * chunks;
-       item += nwarps) {
+  // T * chunks < 2^31 (checked by the launcher): 32-bit index arithmetic
+  const uint32_t chunks = static_cast<uint32_t>((H + 255) / 256);
+  const uint32_t total = static_cast<uint32_t>(T) * chunks;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (uint32_t item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < total; item += nwarps) {
     const int64_t t = item / chunks;
-    const int64_t ch = item - t * chunks;
+    const int64_t ch = item - static_cast<uint32_t>(t) * chunks;
     const int64_t k0 = ch * 256 + lane * 8;
     const bool real = k0 < H;
     float v[8];
@@ -244,6 +245,7 @@ cudaError_t launch_moe_align(const int32_t* ids, int64_t T, int topk, int E, con
 cudaError_t launch_moe_quant_permute(const void* x, int64_t T, int64_t H, int topk, const float* d_g,
                                      const MoEWorkspace& w, int num_sms, cudaStream_t stream) {
   const int64_t items = T * ((H + 255) / 256);
+  if (items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   int64_t blocks = (items + 7) / 8;
   const int64_t cap = static_cast<int64_t>(num_sms) * 16;
   if (blocks > cap) blocks = cap;

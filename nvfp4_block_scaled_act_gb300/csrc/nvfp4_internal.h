@@ -10,7 +10,7 @@ namespace nvfp4 {
 
 // ---- quantisation (quant.cu) ----------------------------------------------
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, const float* d_global,
-                             uint8_t* codes, uint8_t* scales, cudaStream_t stream);
+                             uint8_t* codes, uint8_t* scales, int num_sms, cudaStream_t stream);
 cudaError_t launch_compute_global(const void* x, int64_t rows, int64_t cols, int64_t ldx, float* d_global,
                                   cudaStream_t stream, int num_sms);
 cudaError_t launch_make_alpha(const float* d_g_a, const float* d_g_w, int64_t n, float* d_alpha,

@@ -13,61 +13,113 @@
 
 namespace nvfp4 {
 
-constexpr int kQuantUnroll = 4;  // chunks per warp, loads issued together
+constexpr int kQuantUnroll = 4;  // chunks per warp and iteration, loads issued together
+
+// Work item = kQuantUnroll consecutive 256-element chunks of one row (padded
+// rows and columns included), so one 32-bit division per item finds its row.
+// The grid is persistent; each warp loads its next item while it converts
+// the current one.
+struct QuantItem {
+  uint4 raw[kQuantUnroll];
+};
+
+__device__ __forceinline__ void quant_load_item(QuantItem& it, uint32_t item, uint32_t total, uint32_t groups,
+                                                uint32_t chunks, const uint16_t* __restrict__ x, int64_t M,
+                                                int64_t ldx, int64_t C, int lane) {
+  const uint32_t r32 = item / groups;
+  const uint32_t ch0 = (item - r32 * groups) * kQuantUnroll;
+  const bool row_real = item < total && static_cast<int64_t>(r32) < M;
+  const uint16_t* xrow = x + static_cast<int64_t>(r32) * ldx;
+#pragma unroll
+  for (int u = 0; u < kQuantUnroll; ++u) {
+    const uint32_t ch = ch0 + u;
+    const int64_t cc = static_cast<int64_t>(ch) * 16 + (lane >> 1);
+    it.raw[u] = (row_real && ch < chunks && cc < C)
+                    ? __ldg(reinterpret_cast<const uint4*>(xrow + static_cast<int64_t>(ch) * 256 + lane * 8))
+                    : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Eight fp32 -> four bytes of e2m1 codes (element 2j in the low nibble of byte j).
+__device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float (&v)[8], float r) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(out)
+      : "f"(__fmul_rn(v[0], r)), "f"(__fmul_rn(v[1], r)), "f"(__fmul_rn(v[2], r)), "f"(__fmul_rn(v[3], r)),
+        "f"(__fmul_rn(v[4], r)), "f"(__fmul_rn(v[5], r)), "f"(__fmul_rn(v[6], r)), "f"(__fmul_rn(v[7], r)));
+  return out;
+}
 
 __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                         int64_t ldx, const float* __restrict__ d_global,
                                                         uint8_t* __restrict__ codes,
                                                         uint8_t* __restrict__ scales, int64_t Mp, int64_t C,
                                                         int64_t Cp) {
+  // r = g / S for every E4M3 scale byte S (IEEE division, as in the block rule)
+  __shared__ float r_of_s8[256];
   const float g = __ldg(d_global);
+  {
+    const float S = e4m3_to_f32(threadIdx.x);
+    r_of_s8[threadIdx.x] = (S != 0.0f && S == S) ? __fdiv_rn(g, S) : 0.0f;
+  }
+  __syncthreads();
   const int lane = threadIdx.x & 31;
-  const int64_t chunks = (Cp * 16 + 255) / 256;  // per row, padded columns included
-  const int64_t total = Mp * chunks;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const uint32_t chunks = static_cast<uint32_t>((Cp * 16 + 255) / 256);  // per row
+  const uint32_t groups = (chunks + kQuantUnroll - 1) / kQuantUnroll;   // per row
+  const uint32_t total = static_cast<uint32_t>(Mp) * groups;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
   const int64_t cpad4 = Cp / 4;
-  for (int64_t base = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * kQuantUnroll;
-       base < total; base += nwarps * kQuantUnroll) {
-    uint4 raw[kQuantUnroll];
-    int64_t rr[kQuantUnroll], cc[kQuantUnroll], kk[kQuantUnroll];
-    bool real[kQuantUnroll];
+  uint32_t item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  QuantItem cur;
+  quant_load_item(cur, item, total, groups, chunks, x, M, ldx, C, lane);
+  for (; item < total; item += nwarps) {
+    QuantItem nxt;
+    quant_load_item(nxt, item + nwarps, total, groups, chunks, x, M, ldx, C, lane);
+    const uint32_t r32 = item / groups;
+    const uint32_t ch0 = (item - r32 * groups) * kQuantUnroll;
+    const int64_t r = r32;
+    const bool row_real = r < M;
+    uint8_t* crow = codes + r * (K / 2);
+    uint8_t* srow = scales + ((r >> 7) * cpad4) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      const int64_t item = base + u;
-      const int64_t r = item / chunks;
-      const int64_t ch = item - r * chunks;
-      rr[u] = r;
-      cc[u] = ch * 16 + (lane >> 1);
-      kk[u] = ch * 256 + lane * 8;
-      real[u] = (item < total) && (r < M) && (cc[u] < C);
-      raw[u] = real[u] ? __ldg(reinterpret_cast<const uint4*>(x + r * ldx + kk[u])) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-      float v[8];
-      float amax = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        v[2 * j] = bf16_bits_to_f32(w[j] & 0xFFFFu);
-        v[2 * j + 1] = bf16_bits_to_f32(w[j] >> 16);
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+      const uint32_t ch = ch0 + u;
+      if (ch >= chunks) break;  // warp-uniform
+      const uint32_t cc = ch * 16 + (lane >> 1);  // scale column of this lane's block
+      const bool real = row_real && cc < C;
+      const uint32_t w[4] = {cur.raw[u].x, cur.raw[u].y, cur.raw[u].z, cur.raw[u].w};
+      // block amax on packed bf16 magnitudes (the max of bf16 values is exact;
+      // like fmaxf, __hmax2 returns the other operand when one is NaN)
+      const uint32_t m0 = w[0] & 0x7FFF7FFFu, m1 = w[1] & 0x7FFF7FFFu;
+      const uint32_t m2 = w[2] & 0x7FFF7FFFu, m3 = w[3] & 0x7FFF7FFFu;
+      const __nv_bfloat162 x01 = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&m0),
+                                         *reinterpret_cast<const __nv_bfloat162*>(&m1));
+      const __nv_bfloat162 x23 = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&m2),
+                                         *reinterpret_cast<const __nv_bfloat162*>(&m3));
+      const __nv_bfloat162 xm = __hmax2(x01, x23);
+      const uint32_t a01 = *reinterpret_cast<const uint32_t*>(&xm);
+      float amax = fmaxf(bf16_bits_to_f32(a01 & 0xFFFFu), bf16_bits_to_f32(a01 >> 16));
       amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-      const BlockScale bs = block_scale(amax, g);
-      if (real[u]) {
-        uint32_t packed = 0;
-        if (bs.r != 0.0f) {
+      const uint32_t s8 = f32_to_e4m3(__fmul_rn(__fdiv_rn(amax, 6.0f), g));
+      const float rr = r_of_s8[s8];
+      if (real) {
+        float v[8];
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            packed |= f32x2_to_e2m1x2(__fmul_rn(v[2 * j], bs.r), __fmul_rn(v[2 * j + 1], bs.r)) << (8 * j);
+        for (int j = 0; j < 4; ++j) {
+          v[2 * j] = bf16_bits_to_f32(w[j] & 0xFFFFu);
+          v[2 * j + 1] = bf16_bits_to_f32(w[j] >> 16);
         }
-        *reinterpret_cast<uint32_t*>(codes + rr[u] * (K / 2) + kk[u] / 2) = packed;
+        const uint32_t packed = (rr != 0.0f) ? f32x8_to_e2m1x8(v, rr) : 0u;
+        *reinterpret_cast<uint32_t*>(crow + ch * 128 + lane * 4) = packed;
       }
-      if ((lane & 1) == 0 && base + u < total && rr[u] < Mp && cc[u] < Cp)
-        scales[sf_offset(rr[u], cc[u], cpad4)] = real[u] ? static_cast<uint8_t>(bs.s8) : 0;
+      if ((lane & 1) == 0 && cc < Cp) srow[(cc >> 2) * 512 + (cc & 3)] = real ? static_cast<uint8_t>(s8) : 0;
     }
+    cur = nxt;
   }
 }
 
@@ -137,11 +189,15 @@ __global__ void __launch_bounds__(256) reduce_max_kernel(const float* __restrict
 }
 
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, const float* d_global,
-                             uint8_t* codes, uint8_t* scales, cudaStream_t stream) {
+                             uint8_t* codes, uint8_t* scales, int num_sms, cudaStream_t stream) {
   const int64_t C = K / 16, Cp = (C + 3) / 4 * 4, Mp = (M + 127) / 128 * 128;
-  const int64_t items = Mp * ((Cp * 16 + 255) / 256);
-  const int64_t want = (items + 8 * kQuantUnroll - 1) / (8 * kQuantUnroll);
-  const int blocks = static_cast<int>(want < 1 ? 1 : (want > 65535 ? 65535 : want));
+  const int64_t chunks = (Cp * 16 + 255) / 256;
+  const int64_t items = Mp * ((chunks + kQuantUnroll - 1) / kQuantUnroll);  // warp work items
+  if (items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+  // persistent: 4 blocks of 8 warps per SM (the register limit at 256 threads)
+  const int64_t want = (items + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 4;
+  const int blocks = static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
   quant_act_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), M, K, ldx, d_global, codes, scales,
                                                Mp, C, Cp);
   return cudaGetLastError();
