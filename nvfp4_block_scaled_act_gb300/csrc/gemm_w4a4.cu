@@ -54,7 +54,11 @@ struct GemmCfg {
   static constexpr int SFA_BYTES = 2048;   // 4 atoms = 256 k of 128 rows
   static constexpr int SFB_BYTES = NBLK * 2048;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+  // MoE down: fp32 staging of each epilogue warp's 32 rows x BN/2 columns (row
+  // pitch padded by 16 bytes) for the bulk reduce-add into y
+  static constexpr int EPI_PITCH = (BN / 2) * 4 + 16;
+  static constexpr int EPI_BYTES = MODE_ == 3 ? 8 * 32 * EPI_PITCH : 0;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024;
   static constexpr int SF_COLS = 16 + 4 * (BN / 32);  // TMEM scale columns per stage
   static constexpr int SF_BASE = NUM_ACC * BN;
   static constexpr int TMEM_COLS = 512;
@@ -68,7 +72,10 @@ struct GemmCfg {
 // ---------------------------------------------------------------------------
 // epilogue helpers
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float silu_f32(float v) { return __fdiv_rn(v, __fadd_rn(1.0f, expf(-v))); }
+// silu(v) = v / (1 + e^-v) with the hardware exp2 and fast division (a few ulp
+// from the correctly rounded value; both the calibration and the quantising
+// epilogue use it).
+__device__ __forceinline__ float silu_f32(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -103,9 +110,25 @@ __device__ __forceinline__ void red_add_32(float* dst, const uint32_t (&r)[32], 
                __uint_as_float(r[4 * v + 2]) * scale, __uint_as_float(r[4 * v + 3]) * scale);
 }
 
+// Bulk reduce-add of `bytes` fp32 from shared memory into global memory
+// (both 16-byte aligned, bytes % 16 == 0), in this thread's bulk group.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const float* ssrc, uint32_t bytes) {
+  asm volatile(
+      "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;\n\t"
+      "cp.async.bulk.commit_group;" ::"l"(gdst),
+      "r"(smem_u32(ssrc)), "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Quantise 64 consecutive h values (four 16-blocks) of one row: 32 code bytes
-// and 4 scale bytes.
-__device__ __forceinline__ void quant64(const float (&h)[64], float g, uint4& c0, uint4& c1, uint32_t& s4) {
+// and 4 scale bytes.  r_of_s8[s] = g / S(s) (IEEE division, per E4M3 byte).
+__device__ __forceinline__ void quant64(const float (&h)[64], float g, const float* r_of_s8, uint4& c0, uint4& c1,
+                                        uint32_t& s4) {
   uint32_t words[8];
   s4 = 0;
 #pragma unroll
@@ -117,7 +140,9 @@ __device__ __forceinline__ void quant64(const float (&h)[64], float g, uint4& c0
       v[i] = h[16 * b + i];
       amax = fmaxf(amax, fabsf(v[i]));
     }
-    const BlockScale bs = block_scale(amax, g);
+    BlockScale bs;
+    bs.s8 = f32_to_e4m3(__fmul_rn(__fdiv_rn(amax, 6.0f), g));
+    bs.r = r_of_s8[bs.s8];
     const uint2 w = encode_block16(v, bs.r, bs.r == 0.0f);
     words[2 * b] = w.x;
     words[2 * b + 1] = w.y;
@@ -165,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t done_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
+  __shared__ float r_of_s8[MODE == kEpiGatedQuant ? 256 : 1];  // g_out / S for every E4M3 scale byte
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -186,6 +212,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+  }
+  if constexpr (MODE == kEpiGatedQuant) {
+    if (threadIdx.x < 256) {
+      const float S = e4m3_to_f32(threadIdx.x);
+      r_of_s8[threadIdx.x] = (S != 0.0f && S == S) ? __fdiv_rn(__ldg(p.g_out), S) : 0.0f;
+    }
   }
   if (warp == 1) {
     tmem_alloc(&tmem_slot, Cfg::TMEM_COLS);
@@ -447,14 +479,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < COLS / 32; ++c) store_bf16_32(dst + 32 * c, r[c], alpha_dense, p.N - nbase - 32 * c);
           }
         } else {
+          // w * alpha_e * acc of this row -> the warp's staging row -> one bulk
+          // reduce-add (fp32) into the token's row of y
           const int prow = mt * 128 + row;
           const int rm = p.row_map[prow];
+          float* stg = reinterpret_cast<float*>(smem + STAGES * Cfg::STAGE_BYTES + (ew * 32 + lane) * Cfg::EPI_PITCH);
+          bulk_wait_read_all();  // this lane's previous reduce has read its staging row
           if (rm >= 0) {
             const int e = p.tile_expert[mt];
             const float scale = __fmul_rn(__ldg(p.topk_w + rm), __ldg(p.alpha + e));
-            float* dst = p.y + static_cast<int64_t>(rm / p.topk) * p.ldy + nt * BN + part * COLS;
 #pragma unroll
-            for (int c = 0; c < COLS / 32; ++c) red_add_32(dst + 32 * c, r[c], scale);
+            for (int c = 0; c < COLS / 32; ++c)
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                reinterpret_cast<float4*>(stg + 32 * c)[v] =
+                    make_float4(__uint_as_float(r[c][4 * v]) * scale, __uint_as_float(r[c][4 * v + 1]) * scale,
+                                __uint_as_float(r[c][4 * v + 2]) * scale, __uint_as_float(r[c][4 * v + 3]) * scale);
+            fence_proxy_async_smem();
+            bulk_reduce_add_f32(p.y + static_cast<int64_t>(rm / p.topk) * p.ldy + nt * BN + part * COLS, stg,
+                                COLS * 4);
           }
         }
       } else {
@@ -484,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (rm >= 0) {
             uint4 c0, c1;
             uint32_t s4;
-            quant64(h, g_out, c0, c1, s4);
+            quant64(h, g_out, r_of_s8, c0, c1, s4);
             uint8_t* dst = p.q_codes + static_cast<int64_t>(prow) * p.q_row_bytes + nt * 64 + part * 32;
             reinterpret_cast<uint4*>(dst)[0] = c0;
             reinterpret_cast<uint4*>(dst)[1] = c1;
@@ -509,6 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if constexpr (MODE == kEpiDownSum) bulk_wait_all();  // this thread's reduce-adds into y are complete
   tc_fence_before();
   __syncthreads();
   if constexpr (Cfg::CL > 1) cluster_sync();  // no peer arrives or writes into this CTA after this point
@@ -526,7 +570,7 @@ using Dense2Cfg = GemmCfg<256, 1, 4, kEpiDense, 2>;
 using Dense4Cfg = GemmCfg<256, 1, 4, kEpiDense, 4>;
 using GatedCfg = GemmCfg<256, 1, 4, kEpiGatedQuant>;
 using AmaxCfg = GemmCfg<256, 1, 4, kEpiGatedAmax>;
-using DownCfg = GemmCfg<128, 2, 6, kEpiDownSum>;
+using DownCfg = GemmCfg<128, 2, 4, kEpiDownSum>;
 
 template <class Cfg>
 static cudaError_t launch_cfg(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {
