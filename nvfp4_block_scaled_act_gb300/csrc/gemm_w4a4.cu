@@ -455,10 +455,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float g_out = (MODE == kEpiGatedQuant) ? __ldg(p.g_out) : 0.0f;
     for (int tile = unit0; tile < total; tile += unit_step) {
       const int mg = tile / p.n_tiles, nt = tile - mg * p.n_tiles;
-        const int mt = mg * Cfg::CL + rank;
+      const int mt = mg * Cfg::CL + rank;
+      const int row = 32 * q + lane;
+      // per-row routing data of a grouped tile, loaded while the MMAs run
+      int rm = -1, e = 0;
+      float row_scale = 0.0f;
+      if constexpr (Cfg::GROUPED) {
+        rm = p.row_map[mt * 128 + row];
+        e = p.tile_expert[mt];
+        const float ae = __ldg(p.alpha + e);
+        row_scale = (MODE == kEpiDownSum && rm >= 0) ? __fmul_rn(__ldg(p.topk_w + rm), ae) : ae;
+      }
       if (!mbar_wait(&accf_bar[acc], acc_phase, &abort_flag, p.status)) break;
       tc_fence_after();
-      const int row = 32 * q + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
 
       if constexpr (MODE == kEpiDense || MODE == kEpiDownSum) {
@@ -481,13 +490,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           // w * alpha_e * acc of this row -> the warp's staging row -> one bulk
           // reduce-add (fp32) into the token's row of y
-          const int prow = mt * 128 + row;
-          const int rm = p.row_map[prow];
           float* stg = reinterpret_cast<float*>(smem + STAGES * Cfg::STAGE_BYTES + (ew * 32 + lane) * Cfg::EPI_PITCH);
           bulk_wait_read_all();  // this lane's previous reduce has read its staging row
           if (rm >= 0) {
-            const int e = p.tile_expert[mt];
-            const float scale = __fmul_rn(__ldg(p.topk_w + rm), __ldg(p.alpha + e));
+            const float scale = row_scale;
 #pragma unroll
             for (int c = 0; c < COLS / 32; ++c)
 #pragma unroll
@@ -513,9 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&acce_bar[acc]);
         const int prow = mt * 128 + row;
-        const int rm = p.row_map[prow];
-        const int e = p.tile_expert[mt];
-        const float a = __ldg(p.alpha + e);
+        const float a = row_scale;
         float h[64];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {

@@ -320,6 +320,16 @@ __device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t ran
   return v;
 }
 
+__device__ __forceinline__ void cp_async_16(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sdst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Power-of-two exponent that puts a token's largest magnitude (fp32 bits) in
 // [2^14, 2^15), clamped so that 2^shift and 2^-shift stay normal floats.
 __device__ __forceinline__ int token_shift(unsigned int amax_bits) {
@@ -354,7 +364,7 @@ __global__ void __launch_bounds__(kRingThreads) gemv_ring_kernel(
   uint8_t* ring_sf = ring + R * kRingChunk;                       // R x scales
   const int xs_stride = kc * 2 + 16;
   uint8_t* xs = ring_sf + R * kRingChunkSf;                       // [T][kc*2+16] f16 activations
-  float* part = reinterpret_cast<float*>(xs + T * xs_stride);     // [2][T][128] partial sums
+  float* part = reinterpret_cast<float*>(xs + T * xs_stride);     // [T][128] partial sums
   const uint8_t* sf_src = w_sf + (static_cast<int64_t>(rb) * (K / 64) + k_begin / 64) * 512;
 
   if (threadIdx.x == 0) {
@@ -382,53 +392,50 @@ __global__ void __launch_bounds__(kRingThreads) gemv_ring_kernel(
   // activations, alpha and the output follow the preceding kernel
   pdl_wait();
   const float alpha = __ldg(d_alpha);
-  const int units = k_len / 8;  // 16-byte activation units per token (a multiple of 16)
+  const int units = k_len / 8;  // 16-byte activation units per token
   constexpr int kComp = kRingWarps * 32;
+  const int nunits = T * units;
   if (warp < kRingWarps) {
-    constexpr int kXB = 4;
-    for (int u0 = threadIdx.x; u0 - static_cast<int>(threadIdx.x) < T * units; u0 += kXB * kComp) {
-      uint4 v[kXB];
-#pragma unroll
-      for (int q = 0; q < kXB; ++q) {
-        const int u = u0 + q * kComp;
-        v[q] = make_uint4(0u, 0u, 0u, 0u);
-        if (u < T * units) {
-          const int tok = u / units;
-          v[q] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * ldx + k_begin +
-                                                      (u - tok * units) * 8));
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < kXB; ++q) {
-        const int ubase = u0 + q * kComp - lane;  // first unit of this warp (warp-uniform)
-        if (ubase >= T * units) break;
-        const int u = ubase + lane;
-        const bool in = u < T * units;
-        const int tok = in ? u / units : T;
-        const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-        float m = 0.0f;
+    // raw bf16 straight into the permuted slots, every copy in flight at once
+    for (int u = threadIdx.x; u < nunits; u += kComp) {
+      const int tok = u / units;
+      const int k8 = (u - tok * units) * 8;
+      cp_async_16(xs + tok * xs_stride + (k8 >> 7) * 256 + xchunk((k8 & 127) >> 3) * 16,
+                  x + static_cast<int64_t>(tok) * ldx + k_begin + k8);
+    }
+    cp_async_wait_all();
+  }
+  __syncthreads();
+  if (warp < kRingWarps) {
+    // token amax: the 32 units of a warp span at most three tokens (units is a
+    // multiple of 16); one warp max and one shared atomic per token spanned
+    for (int ubase = threadIdx.x - lane; ubase < nunits; ubase += kComp) {
+      const int u = ubase + lane;
+      const bool in = u < nunits;
+      const int tok = in ? u / units : T;
+      float m = 0.0f;
+      if (in) {
+        const int k8 = (u - tok * units) * 8;
+        const uint4 v = *reinterpret_cast<const uint4*>(xs + tok * xs_stride + (k8 >> 7) * 256 +
+                                                        xchunk((k8 & 127) >> 3) * 16);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           m = fmaxf(m, fabsf(bf16_bits_to_f32(w4[e] & 0xFFFFu)));
           m = fmaxf(m, fabsf(bf16_bits_to_f32(w4[e] >> 16)));
         }
-        // the 32 units of a warp span at most three tokens
-        const int t0 = ubase / units, t1 = min(T - 1, (ubase + 31) / units);
-        for (int tt = t0; tt <= t1; ++tt) {
-          const unsigned int mb = __reduce_max_sync(0xFFFFFFFFu, (in && tok == tt) ? __float_as_uint(m) : 0u);
-          if (lane == 0 && mb != 0u) atomicMax(&tok_amax[tt], mb);
-        }
-        if (in) {
-          const int k8 = (u - tok * units) * 8;
-          *reinterpret_cast<uint4*>(xs + tok * xs_stride + (k8 >> 7) * 256 + xchunk((k8 & 127) >> 3) * 16) = v[q];
-        }
+      }
+      const int t0 = ubase / units, t1 = min(T - 1, (ubase + 31) / units);
+      for (int tt = t0; tt <= t1; ++tt) {
+        const unsigned int mb = __reduce_max_sync(0xFFFFFFFFu, (in && tok == tt) ? __float_as_uint(m) : 0u);
+        if (lane == 0 && mb != 0u) atomicMax(&tok_amax[tt], mb);
       }
     }
   }
   __syncthreads();
   if (warp < kRingWarps) {
     // in place: bf16 -> f16 after the token's power-of-two rescale
-    for (int u = threadIdx.x; u < T * units; u += kComp) {
+    for (int u = threadIdx.x; u < nunits; u += kComp) {
       const int tok = u / units;
       const float f = pow2f(-token_shift(tok_amax[tok]));
       const int k8 = (u - tok * units) * 8;
@@ -438,7 +445,8 @@ __global__ void __launch_bounds__(kRingThreads) gemv_ring_kernel(
       uint32_t o[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const __half2 h = __floats2half2_rn(bf16_bits_to_f32(w4[e] & 0xFFFFu) * f, bf16_bits_to_f32(w4[e] >> 16) * f);
+        const __half2 h =
+            __floats2half2_rn(bf16_bits_to_f32(w4[e] & 0xFFFFu) * f, bf16_bits_to_f32(w4[e] >> 16) * f);
         o[e] = *reinterpret_cast<const uint32_t*>(&h);
       }
       *slot = make_uint4(o[0], o[1], o[2], o[3]);
@@ -536,17 +544,36 @@ __global__ void __launch_bounds__(kRingThreads) gemv_ring_kernel(
         }
       }
     }
-    // partials with the rescale undone -> part[kp][tok][row]
+    // partials with the rescale undone: k-parity 1 -> part, then parity 0 adds
+    // its own (after the compute warps' barrier) -> part[tok][row]
+    if (kp == 1) {
 #pragma unroll
-    for (int a = 0; a < 2; ++a)
+      for (int a = 0; a < 2; ++a)
 #pragma unroll
-      for (int h = 0; h < (kTok16 ? 2 : 1); ++h)
+        for (int h = 0; h < (kTok16 ? 2 : 1); ++h)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int row = lr0 + a * 16 + g + 8 * (c >> 1);
-          const int tok = h * 8 + 2 * t + (c & 1);
-          if (tok < T) part[(kp * T + tok) * kRingRows + row] = acc[a][h][c] * pow2f(token_shift(tok_amax[tok]));
-        }
+          for (int c = 0; c < 4; ++c) {
+            const int row = lr0 + a * 16 + g + 8 * (c >> 1);
+            const int tok = h * 8 + 2 * t + (c & 1);
+            if (tok < T) part[tok * kRingRows + row] = acc[a][h][c] * pow2f(token_shift(tok_amax[tok]));
+          }
+    }
+    named_barrier_sync(1, kComp);
+    if (kp == 0) {
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int h = 0; h < (kTok16 ? 2 : 1); ++h)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int row = lr0 + a * 16 + g + 8 * (c >> 1);
+            const int tok = h * 8 + 2 * t + (c & 1);
+            if (tok < T) {
+              float* pp = part + tok * kRingRows + row;
+              *pp = __fadd_rn(acc[a][h][c] * pow2f(token_shift(tok_amax[tok])), *pp);
+            }
+          }
+    }
   }
   __syncthreads();
   if (abort_flag && producer) {
@@ -567,15 +594,13 @@ __global__ void __launch_bounds__(kRingThreads) gemv_ring_kernel(
     const int tok = e / rows_per;
     const int row = static_cast<int>(rank) * rows_per + (e - tok * rows_per);
     if (row >= kRingRows) continue;
-    float v[2 * kRingMaxCluster];
+    float v[kRingMaxCluster];
 #pragma unroll
-    for (int q = 0; q < kRingMaxCluster; ++q) {
-      v[2 * q] = q < static_cast<int>(ncl) ? ld_cluster_f32(part + tok * kRingRows + row, q) : 0.0f;
-      v[2 * q + 1] = q < static_cast<int>(ncl) ? ld_cluster_f32(part + (T + tok) * kRingRows + row, q) : 0.0f;
-    }
+    for (int q = 0; q < kRingMaxCluster; ++q)
+      v[q] = q < static_cast<int>(ncl) ? ld_cluster_f32(part + tok * kRingRows + row, q) : 0.0f;
     float sum = 0.0f;
 #pragma unroll
-    for (int q = 0; q < 2 * kRingMaxCluster; ++q) sum += v[q];
+    for (int q = 0; q < kRingMaxCluster; ++q) sum += v[q];
     const int n = rb * kRingRows + row;
     if (n < N) out[static_cast<int64_t>(tok) * ldo + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum * alpha));
   }
@@ -594,7 +619,7 @@ GemvRingPlan gemv_ring_plan(int64_t T, int64_t N, int64_t K, int num_sms) {
   p.cl = static_cast<int>(cl);
   p.kc = static_cast<int>(kcb * 128);
   p.row_blocks = row_blocks;
-  const size_t fixed = static_cast<size_t>(T) * (kcb * 256 + 16) + static_cast<size_t>(2 * T * kRingRows * 4);
+  const size_t fixed = static_cast<size_t>(T) * (kcb * 256 + 16) + static_cast<size_t>(T * kRingRows * 4);
   int64_t slots = fixed < kRingSmemBudget ? static_cast<int64_t>((kRingSmemBudget - fixed) / kRingSlot) : 0;
   if (slots > kcb) slots = kcb;
   if (slots > kRingMaxSlots) slots = kRingMaxSlots;
