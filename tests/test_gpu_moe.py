@@ -162,7 +162,7 @@ def test_moe_config_small_tokens(nv, T):
     check_close(out, m.run_oracle(), f"MoE E=128 T={T}")
 
 
-@pytest.mark.parametrize("T", [1024, 4096])
+@pytest.mark.parametrize("T", [1024, 4096, 8192])
 def test_moe_config_sampled_tokens(nv, T):
     """E = 128, top-8 at the larger T: the whole layer on the GPU, the oracle on a
     seeded sample of 48 tokens (tokens are independent)."""
