@@ -351,7 +351,7 @@ def run_ours(args, world, rank, local):
                      "peak_source": f"{peak_src} copy bandwidth",
                      "algorithmic_bytes_per_launch": head_bytes, "launch_us": round(head["us"], 3),
                      "traffic": _profile_traffic("gemv_w4a16_T1_8704x5120.md")},
-        "roofline_gemm": {"kernel": "gemm_nvfp4_kernel (W4A4, M=8192)", "bound": "tensor",
+        "roofline_gemm": {"kernel": "gemm_pair_kernel (W4A4, M=8192, CTA pairs)", "bound": "tensor",
                           "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                           "frac": round(gemm_tflops / fp4_peak, 4),
                           "peak_source": f"{peak_src} bf16 burst {bf16} TFLOP/s x {FP4_OVER_BF16:g} (nominal FP4:BF16)",

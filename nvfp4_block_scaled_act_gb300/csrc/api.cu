@@ -78,22 +78,6 @@ inline nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// CTAs per cluster that share each 256-row weight tile of the dense W4A4 GEMM
-// through TMA multicast.  Multicast cuts the L2 -> SM traffic of the weight,
-// but every CTA still holds the whole tile in shared memory, and measured on
-// GB300 (M = 512 ... 8192, N = 7168, K = 5120) 2 and 4 gave no gain over 1, so
-// 1 is the default.  NVFP4_DENSE_CLUSTER = 1, 2 or 4 selects another size.
-int dense_cluster(int64_t m_tiles) {
-  static int forced = -1;
-  if (forced < 0) {
-    const char* env = std::getenv("NVFP4_DENSE_CLUSTER");
-    const int v = env ? std::atoi(env) : 0;
-    forced = (v == 1 || v == 2 || v == 4) ? v : 0;
-  }
-  if (forced > 0 && m_tiles >= forced) return forced;
-  return 1;
-}
-
 }  // namespace
 
 // Codes of the decode weight: boxes of 64 bytes (one 128-k block) x 128 rows,
@@ -119,6 +103,18 @@ bool make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t ro
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -276,9 +272,9 @@ nvfp4_status nvfp4_linear_w4a4(const uint8_t* a_codes, const uint8_t* a_sf, int6
   const DeviceInfo* dev = device_info();
   if (!dev) return NVFP4_ERR_NO_DEVICE;
   const int64_t m_tiles = (M + 127) / 128;
-  const int cl = dense_cluster(m_tiles);
   GemmMaps maps;
-  if (!make_codes_map(&maps.a, a_codes, M, K / 2) || !make_codes_map(&maps.b, w_codes, N, K / 2, cl == 1 ? 128 : 256 / cl))
+  if (!make_codes_map(&maps.a, a_codes, M, K / 2) || !make_codes_map(&maps.b, w_codes, N, K / 2) ||
+      !make_out_map(&maps.out, out, M, N, ldo))
     return NVFP4_ERR_CUDA;
   GemmParams p{};
   p.sfa = a_sf;
@@ -295,9 +291,10 @@ nvfp4_status nvfp4_linear_w4a4(const uint8_t* a_codes, const uint8_t* a_sf, int6
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.status = dev->status;
-  const int64_t units = ((m_tiles + cl - 1) / cl) * p.n_tiles;
-  const int64_t clusters = units < dev->sms / cl ? units : dev->sms / cl;
-  return cuda_status(launch_gemm(kEpiDense, maps, p, static_cast<int>(clusters * cl), stream, cl));
+  // one CTA pair per 256 x 256 tile, at most one pair per two SMs
+  const int64_t units = ((m_tiles + 1) / 2) * p.n_tiles;
+  const int64_t pairs = units < dev->sms / 2 ? units : dev->sms / 2;
+  return cuda_status(launch_gemm(kEpiDense, maps, p, static_cast<int>(2 * pairs), stream));
 }
 
 size_t nvfp4_linear_w4a16_workspace(int64_t T, int64_t N, int64_t K) {

@@ -16,10 +16,19 @@
 // section "Changes") were written for mma.sync on sm_120; this kernel keeps
 // their dataflow and epilogue fusion and maps it onto tcgen05 and TMEM.
 //
-// Structure (one CTA of 16 warps per SM, persistent over tiles n-fastest):
-//   warp 0      TMA producer: a 128x128-byte A box, BN/128 B boxes (128-byte
-//               swizzle) and the matching 512-byte scale atoms (bulk copies,
-//               contiguous in the 128x4 layout) into a STAGES-deep smem ring.
+// Two kernels.  gemm_nvfp4_kernel (below) runs one CTA per SM on 128 x BN tiles
+// and serves the grouped MoE GEMMs; gemm_pair_kernel (further down) runs the
+// dense W4A4 linear on CTA pairs and 256 x 256 tiles.
+//
+// gemm_nvfp4_kernel structure (one CTA of 16 warps per SM, persistent over
+// tiles n-fastest):
+//   warp 0      operand producer: a 128x128-byte A box and the B tile (one
+//               BN-row box, or one 128-row box per block for the MoE gate
+//               and up blocks; 128-byte swizzle) into a STAGES-deep smem ring.
+//   warp 2      scale producer: the stage's 512-byte scale atoms of A and B
+//               (bulk copies, contiguous in the 128x4 layout).  Splitting the
+//               copies over two warps halves the serial issue work per stage
+//               (each TMA or bulk copy costs its issuing lane about 100 cycles).
 //   warp 1      allocates TMEM; one lane issues 4 MMAs of K = 64 per 256-k
 //               stage once the stage's scales are in TMEM; tcgen05.commit
 //               releases smem stages and publishes finished accumulators.
@@ -39,14 +48,12 @@
 
 namespace nvfp4 {
 
-template <int BN_, int NUM_ACC_, int STAGES_, int MODE_, int CL_ = 1>
+template <int BN_, int NUM_ACC_, int STAGES_, int MODE_>
 struct GemmCfg {
   static constexpr int BN = BN_;           // MMA N (B rows per tile)
   static constexpr int NUM_ACC = NUM_ACC_;
   static constexpr int STAGES = STAGES_;
   static constexpr int MODE = MODE_;
-  static constexpr int CL = CL_;           // CTAs of a cluster sharing one B tile (multicast)
-  static constexpr int SLICE = BN_ / CL_;  // B rows each CTA of the cluster loads
   static constexpr int BM = 128;
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
@@ -66,7 +73,6 @@ struct GemmCfg {
   static_assert(SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(SMEM_BYTES <= 232448, "smem budget");
-  static_assert(CL == 1 || (MODE == kEpiDense && SLICE % 64 == 0 && CL <= 4), "multicast: dense tiles only");
 };
 
 // ---------------------------------------------------------------------------
@@ -197,9 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full_bar[s], 1);
+      mbar_init(&full_bar[s], 2);  // the operand and the scale producer
       mbar_init(&sf_bar[s], 4);
-      mbar_init(&empty_bar[s], Cfg::CL);
+      mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < NUM_ACC; ++a) {
       mbar_init(&accf_bar[a], 1);
@@ -225,36 +231,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (Cfg::CL > 1) cluster_sync();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = tmem_slot;
 
-  // Work units: a group of CL consecutive 128-row tiles (one per CTA of the
-  // cluster) times one column tile, column-fastest.
+  // Work units: a 128-row tile times a column tile, column-fastest.
   const int m_tiles = Cfg::GROUPED ? *p.d_m_tiles : p.m_tiles;
-  const int rank = (Cfg::CL > 1) ? static_cast<int>(cluster_ctarank()) : 0;
-  const int total = ((m_tiles + Cfg::CL - 1) / Cfg::CL) * p.n_tiles;
-  const int unit0 = blockIdx.x / Cfg::CL;
-  const int unit_step = gridDim.x / Cfg::CL;
-  constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << Cfg::CL) - 1u);
+  const int total = m_tiles * p.n_tiles;
+  const int unit0 = blockIdx.x;
+  const int unit_step = gridDim.x;
   const int wg = warp >> 2;
 
   if (wg == 0) {
     regs_dec();
-    if (warp == 0 && lane == 0) {
-      // ---------------------------------------------------------- producer
-      uint32_t stage = 0, phase = 0;
-      uint32_t last_phase[STAGES];
-      bool issued[STAGES];
-#pragma unroll
-      for (int s = 0; s < STAGES; ++s) {
-        issued[s] = false;
-        last_phase[s] = 0;
-      }
+    if (warp == 0 || warp == 2) {
+      // ---------------------------------------------------------- producers
+      // Warp 0 copies the operand tiles (TMA boxes), warp 2 the scale atoms
+      // (bulk copies); each arrives on the stage's full barrier with its own
+      // byte count, so a stage costs each issuing lane two or three copies.
+      // The whole warp runs the loop, so every address and coordinate is
+      // warp-uniform; lane 0 issues.
+      const bool scale_role = warp == 2;
+      uint32_t it = 0;  // stages issued so far: stage it % STAGES, round it / STAGES
       bool ok = true;
       for (int tile = unit0; ok && tile < total; tile += unit_step) {
-        const int mg = tile / p.n_tiles, nt = tile - mg * p.n_tiles;
-        const int mt = mg * Cfg::CL + rank;
+        const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
         const int e = Cfg::GROUPED ? p.tile_expert[mt] : 0;
         int b_row[Cfg::NBLK];
         if (MODE == kEpiDense) {
@@ -264,8 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           b_row[0] = e * p.b_rows_per_expert + nt * 128;
           if (Cfg::NBLK > 1) b_row[Cfg::NBLK - 1] = b_row[0] + p.up_offset;
         }
+        const bool mvalid = mt < m_tiles;
         for (int kb = 0; kb < p.kblocks; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1, &abort_flag, p.status)) {
+          const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
+          if (!mbar_wait_warp(&empty_bar[stage], phase ^ 1, &abort_flag, p.status)) {
             ok = false;
             break;
           }
@@ -274,66 +276,63 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sB = sA + Cfg::A_BYTES;
           uint8_t* sSFA = sB + Cfg::B_BYTES;
           uint8_t* sSFB = sSFA + Cfg::SFA_BYTES;
-          // bytes landing in this CTA's smem: its own A tile and scales, and the
-          // whole B tile with its scales (from every CTA of the cluster)
-          const bool mvalid = mt < m_tiles;
-          uint32_t bytes = mvalid ? Cfg::A_BYTES + ks * 512 : 0;
+          if (lane == 0) {
+            if (!scale_role) {
+              // A box; B as one BN-row box (dense: consecutive rows) or one
+              // 128-row box per block (gate and up blocks of an expert)
+              uint32_t bytes = mvalid ? Cfg::A_BYTES : 0;
+              if (MODE == kEpiDense) {
+                if (b_row[0] < p.b_rows_total) bytes += Cfg::B_BYTES;
+              } else {
 #pragma unroll
-          for (int j = 0; j < Cfg::NBLK; ++j)
-            if (b_row[j] < p.b_rows_total) bytes += 128 * 128 + ks * 512;
-          mbar_arrive_expect_tx(&full_bar[stage], bytes);
-          if (mvalid) {
-            tma_load_2d(sA, &tmA, &full_bar[stage], kb * 128, mt * 128);
-            bulk_load(sSFA, p.sfa + (static_cast<int64_t>(mt) * p.sf_atoms + kb * 4) * 512, ks * 512,
-                      &full_bar[stage]);
-          }
-          if constexpr (Cfg::CL == 1) {
-#pragma unroll
-            for (int j = 0; j < Cfg::NBLK; ++j) {
-              if (b_row[j] < p.b_rows_total) {
-                tma_load_2d(sB + j * 128 * 128, &tmB, &full_bar[stage], kb * 128, b_row[j]);
-                bulk_load(sSFB + j * 2048,
-                          p.sfb + (static_cast<int64_t>(b_row[j] >> 7) * p.sf_atoms + kb * 4) * 512, ks * 512,
-                          &full_bar[stage]);
+                for (int j = 0; j < Cfg::NBLK; ++j)
+                  if (b_row[j] < p.b_rows_total) bytes += 128 * 128;
               }
-            }
-          } else {
-            // this CTA's slice of B (SLICE rows) and its share of the B scale
-            // atoms, multicast to every CTA of the cluster
-            const int j = (rank * Cfg::SLICE) / 128;
-            if (b_row[j] < p.b_rows_total) {
-              tma_load_2d_mc(sB + rank * Cfg::SLICE * 128, &tmB, &full_bar[stage], kb * 128,
-                             nt * BN + rank * Cfg::SLICE, kClusterMask);
-              constexpr int kRanksPerBlock = Cfg::CL / Cfg::NBLK;
-              constexpr int kAtomsPerRank = 4 / kRanksPerBlock;
-              const int a0 = (rank % kRanksPerBlock) * kAtomsPerRank;
-              const int na = min(ks, a0 + kAtomsPerRank) - a0;
-              if (na > 0)
-                bulk_load_mc(sSFB + j * 2048 + a0 * 512,
-                             p.sfb + (static_cast<int64_t>(b_row[j] >> 7) * p.sf_atoms + kb * 4 + a0) * 512,
-                             na * 512, &full_bar[stage], kClusterMask);
+              mbar_arrive_expect_tx(&full_bar[stage], bytes);
+              if (mvalid) tma_load_2d(sA, &tmA, &full_bar[stage], kb * 128, mt * 128);
+              if (MODE == kEpiDense) {
+                if (b_row[0] < p.b_rows_total) tma_load_2d(sB, &tmB, &full_bar[stage], kb * 128, b_row[0]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < Cfg::NBLK; ++j)
+                  if (b_row[j] < p.b_rows_total) tma_load_2d(sB + j * 128 * 128, &tmB, &full_bar[stage], kb * 128, b_row[j]);
+              }
+            } else {
+              uint32_t bytes = mvalid ? ks * 512 : 0;
+#pragma unroll
+              for (int j = 0; j < Cfg::NBLK; ++j)
+                if (b_row[j] < p.b_rows_total) bytes += ks * 512;
+              mbar_arrive_expect_tx(&full_bar[stage], bytes);
+              if (mvalid)
+                bulk_load(sSFA, p.sfa + (static_cast<int64_t>(mt) * p.sf_atoms + kb * 4) * 512, ks * 512,
+                          &full_bar[stage]);
+#pragma unroll
+              for (int j = 0; j < Cfg::NBLK; ++j)
+                if (b_row[j] < p.b_rows_total)
+                  bulk_load(sSFB + j * 2048, p.sfb + (static_cast<int64_t>(b_row[j] >> 7) * p.sf_atoms + kb * 4) * 512,
+                            ks * 512, &full_bar[stage]);
             }
           }
-          issued[stage] = true;
-          last_phase[stage] = phase;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+          __syncwarp();
+          ++it;
         }
       }
-      // every copy this thread started lands before the CTA can exit
-      // and every release of them (from every CTA of the cluster) has arrived
+      // every copy this warp started lands before the CTA can exit and every
+      // release of its stages has arrived: the last issue of each stage is
+      // among the last STAGES issues
       int drain_abort = 0;
-#pragma unroll
-      for (int s = 0; s < STAGES; ++s)
-        if (issued[s]) {
-          mbar_wait(&full_bar[s], last_phase[s], reinterpret_cast<volatile int*>(&drain_abort), p.status);
-          mbar_wait(&empty_bar[s], last_phase[s], reinterpret_cast<volatile int*>(&drain_abort), p.status);
-        }
+      for (uint32_t i = it > STAGES ? it - STAGES : 0u; i < it; ++i) {
+        mbar_wait_warp(&full_bar[i % STAGES], (i / STAGES) & 1u, reinterpret_cast<volatile int*>(&drain_abort),
+                       p.status);
+        mbar_wait_warp(&empty_bar[i % STAGES], (i / STAGES) & 1u, reinterpret_cast<volatile int*>(&drain_abort),
+                       p.status);
+      }
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
-      if (lane == 0) {
+      // The whole warp runs the loop (descriptors and TMEM addresses are
+      // warp-uniform); lane 0 issues every MMA and commit, since a commit
+      // tracks the MMAs of the thread that issues it.
+      {
         const uint32_t idesc = idesc_nvfp4(128, BN);
         // Descriptors of stage 0; stage s adds s * STAGE_BYTES / 16 to the
         // 14-bit address field (all of shared memory stays below 256 KB).
@@ -342,51 +341,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t db0 = desc_kmajor_sw128(sbase + Cfg::A_BYTES);
         const uint32_t tsf0 = tmem_base + Cfg::SF_BASE;
         constexpr uint32_t kStageUnits = Cfg::STAGE_BYTES >> 4;
-        uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+        uint32_t it = 0, acc = 0, acc_phase = 0;
         bool ok = true;
         for (int tile = unit0; ok && tile < total; tile += unit_step) {
-          if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1, &abort_flag, p.status)) break;
+          if (!mbar_wait_warp(&acce_bar[acc], acc_phase ^ 1, &abort_flag, p.status)) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * BN;
-          for (int kb = 0; kb < p.kblocks; ++kb) {
-            if (!mbar_wait(&sf_bar[stage], phase, &abort_flag, p.status)) {
+          // two 256-k stages per pass: the waits, the fence and the loop are
+          // paid once per eight MMAs, so the lane keeps the tensor pipe fed
+          for (int kb = 0; kb < p.kblocks; kb += 2) {
+            const bool two = kb + 1 < p.kblocks;
+            const uint32_t st0 = it % STAGES, ph0 = (it / STAGES) & 1u;
+            const uint32_t st1 = (it + 1) % STAGES, ph1 = ((it + 1) / STAGES) & 1u;
+            if (!mbar_wait_warp(&sf_bar[st0], ph0, &abort_flag, p.status) ||
+                (two && !mbar_wait_warp(&sf_bar[st1], ph1, &abort_flag, p.status))) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const int ks = min(4, (p.K - kb * 256) >> 6);
-            const uint64_t off = static_cast<uint64_t>(stage * kStageUnits);
-            const uint64_t da = da0 + off, db = db0 + off;
-            const uint32_t t_sfa = tsf0 + stage * Cfg::SF_COLS;
-            const uint32_t t_sfb = t_sfa + 16;
+            if (lane == 0) {
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-              if (s < ks)
-                umma_nvfp4(d_tmem, da + 2 * s, db + 2 * s, idesc, t_sfa + 4 * s, t_sfb + (BN / 32) * s,
-                           (kb > 0 || s > 0) ? 1u : 0u);
+              for (int h = 0; h < 2; ++h) {
+                if (h == 1 && !two) break;
+                const uint32_t stage = h ? st1 : st0;
+                const int ks = min(4, (p.K - (kb + h) * 256) >> 6);
+                const uint64_t off = static_cast<uint64_t>(stage * kStageUnits);
+                const uint64_t da = da0 + off, db = db0 + off;
+                const uint32_t t_sfa = tsf0 + stage * Cfg::SF_COLS;
+                const uint32_t t_sfb = t_sfa + 16;
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                  if (s < ks)
+                    umma_nvfp4(d_tmem, da + 2 * s, db + 2 * s, idesc, t_sfa + 4 * s, t_sfb + (BN / 32) * s,
+                               (kb + h > 0 || s > 0) ? 1u : 0u);
+                }
+                umma_commit(&empty_bar[stage]);
+              }
             }
-            if constexpr (Cfg::CL > 1)
-              umma_commit_mc(&empty_bar[stage], kClusterMask);
-            else
-              umma_commit(&empty_bar[stage]);
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1;
-            }
+            __syncwarp();
+            it += two ? 2u : 1u;
           }
           if (!ok) break;
-          umma_commit(&accf_bar[acc]);
+          if (lane == 0) umma_commit(&accf_bar[acc]);
+          __syncwarp();
           if (++acc == NUM_ACC) {
             acc = 0;
             acc_phase ^= 1;
           }
         }
         // wait until every MMA issued above has completed
-        umma_commit(&done_bar);
+        if (lane == 0) umma_commit(&done_bar);
+        __syncwarp();
         int drain_abort = 0;
-        mbar_wait(&done_bar, 0, reinterpret_cast<volatile int*>(&drain_abort), p.status);
+        mbar_wait_warp(&done_bar, 0, reinterpret_cast<volatile int*>(&drain_abort), p.status);
       }
-      __syncwarp();
     }
   } else if (wg == 1) {
     // ------------------------------------------------------------ scale writers
@@ -454,8 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float alpha_dense = (MODE == kEpiDense) ? __ldg(p.alpha) : 0.0f;
     const float g_out = (MODE == kEpiGatedQuant) ? __ldg(p.g_out) : 0.0f;
     for (int tile = unit0; tile < total; tile += unit_step) {
-      const int mg = tile / p.n_tiles, nt = tile - mg * p.n_tiles;
-      const int mt = mg * Cfg::CL + rank;
+      const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
       const int row = 32 * q + lane;
       // per-row routing data of a grouped tile, loaded while the MMAs run
       int rm = -1, e = 0;
@@ -559,7 +566,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (MODE == kEpiDownSum) bulk_wait_all();  // this thread's reduce-adds into y are complete
   tc_fence_before();
   __syncthreads();
-  if constexpr (Cfg::CL > 1) cluster_sync();  // no peer arrives or writes into this CTA after this point
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
@@ -567,11 +573,335 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// dense W4A4 GEMM on CTA pairs
+// ---------------------------------------------------------------------------
+// A cluster of two CTAs computes a 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 64 per instruction) issued by
+// CTA 0.  CTA r holds rows 128r.. of the A tile and rows 128r.. of the B tile in
+// its shared memory (the MMA reads the peer's halves at the same offsets), its
+// 128 x 256 fp32 accumulator, the scales of its A rows and the scales of all 256
+// B rows in its TMEM.  Against one CTA on a 128 x 256 tile this halves the B
+// bytes an SM brings in per stage (each SM's TMA ingest is what bounds the
+// single-CTA tile), and leaves room to stage the bf16 output tile for TMA stores
+// (row-per-lane global stores scatter 16-byte pieces over 32 rows).
+//
+// Roles per CTA (16 warps):
+//   warp 0      A box and this CTA's 128-row B box of each 256-k stage
+//   warp 2      scale atoms: this CTA's A rows, all 256 B rows
+//   warp 1      TMEM allocation (both CTAs); MMA issue (CTA 0 only)
+//   warps 4-7   scale writers: smem -> own TMEM, then arrive on CTA 0's
+//               scale-ready barrier (8 arrivals: both CTAs)
+//   warps 8-15  epilogue: TMEM -> alpha -> bf16 -> swizzled smem -> TMA store;
+//               the accumulator is released to CTA 0 (16 arrivals) as soon as
+//               it has been read
+// Each CTA's copies complete on its own full barrier; CTA 0's MMA commits are
+// multicast to the stage-empty and accumulator-full barriers of both CTAs.
+struct PairCfg {
+  static constexpr int STAGES = 5;
+  static constexpr int BN = 256;
+  static constexpr int A_BYTES = 128 * 128;   // 128 rows x 256 k
+  static constexpr int B_BYTES = 128 * 128;   // this CTA's 128 B rows
+  static constexpr int SFA_BYTES = 2048;
+  static constexpr int SFB_BYTES = 4096;      // scale atoms of all 256 B rows
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int EPI_WARP_BYTES = 32 * 128;  // one box of 32 rows x 64 bf16 at a time
+  static constexpr int EPI_BYTES = kNumEpi * EPI_WARP_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024;
+  static constexpr int SF_COLS = 48;          // TMEM scale columns per stage: 16 (A) + 32 (B)
+  static constexpr int SF_BASE = BN;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
+  static_assert(STAGE_BYTES % 1024 == 0 && EPI_WARP_BYTES % 1024 == 0, "alignment");
+  static_assert(SMEM_BYTES <= 232448, "smem budget");
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+  using Cfg = PairCfg;
+  constexpr int STAGES = Cfg::STAGES;
+  constexpr int BN = Cfg::BN;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[STAGES];   // this CTA's copies landed
+  __shared__ __align__(8) uint64_t sf_bar[STAGES];     // CTA 0: scales of both CTAs in TMEM
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];  // the stage's MMAs completed
+  __shared__ __align__(8) uint64_t accf_bar;           // the tile's MMAs completed
+  __shared__ __align__(8) uint64_t acce_bar;           // CTA 0: both accumulators read
+  __shared__ __align__(8) uint64_t done_bar;           // CTA 0: every MMA completed
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 2);  // operand and scale producer
+      mbar_init(&sf_bar[s], 8);    // four scale writers in each CTA
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&accf_bar, 1);
+    mbar_init(&acce_bar, 2 * kNumEpi);
+    mbar_init(&done_bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_slot;
+
+  // work units: 256-row tile pairs x 256-column tiles, column-fastest
+  const int m_tiles = p.m_tiles;
+  const int total = ((m_tiles + 1) / 2) * p.n_tiles;
+  const int unit0 = blockIdx.x >> 1;
+  const int unit_step = gridDim.x >> 1;
+  const int wg = warp >> 2;
+
+  if (wg == 0) {
+    regs_dec();
+    if (warp == 0 || warp == 2) {
+      // ---------------------------------------------------------- producers
+      const bool scale_role = warp == 2;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = unit0; ok && tile < total; tile += unit_step) {
+        const int mp = tile / p.n_tiles, nt = tile - mp * p.n_tiles;
+        const int mt = 2 * mp + static_cast<int>(rank);
+        const bool mvalid = mt < m_tiles;
+        const int b_row = nt * BN + 128 * static_cast<int>(rank);
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+          const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
+          if (!mbar_wait_warp(&empty_bar[stage], phase ^ 1, &abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const int ks = min(4, (p.K - kb * 256) / 64);
+          uint8_t* sA = smem + stage * Cfg::STAGE_BYTES;
+          uint8_t* sB = sA + Cfg::A_BYTES;
+          uint8_t* sSFA = sB + Cfg::B_BYTES;
+          uint8_t* sSFB = sSFA + Cfg::SFA_BYTES;
+          if (lane == 0) {
+            if (!scale_role) {
+              const bool bvalid = b_row < p.b_rows_total;
+              mbar_arrive_expect_tx(&full_bar[stage], (mvalid ? Cfg::A_BYTES : 0) + (bvalid ? Cfg::B_BYTES : 0));
+              if (mvalid) tma_load_2d(sA, &tmA, &full_bar[stage], kb * 128, mt * 128);
+              if (bvalid) tma_load_2d(sB, &tmB, &full_bar[stage], kb * 128, b_row);
+            } else {
+              uint32_t bytes = mvalid ? ks * 512 : 0;
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+                if (nt * BN + 128 * j < p.b_rows_total) bytes += ks * 512;
+              mbar_arrive_expect_tx(&full_bar[stage], bytes);
+              if (mvalid)
+                bulk_load(sSFA, p.sfa + (static_cast<int64_t>(mt) * p.sf_atoms + kb * 4) * 512, ks * 512,
+                          &full_bar[stage]);
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+                if (nt * BN + 128 * j < p.b_rows_total)
+                  bulk_load(sSFB + j * 2048, p.sfb + (static_cast<int64_t>(nt * 2 + j) * p.sf_atoms + kb * 4) * 512,
+                            ks * 512, &full_bar[stage]);
+            }
+          }
+          __syncwarp();
+          ++it;
+        }
+      }
+      int drain_abort = 0;
+      for (uint32_t i = it > STAGES ? it - STAGES : 0u; i < it; ++i) {
+        mbar_wait_warp(&full_bar[i % STAGES], (i / STAGES) & 1u, reinterpret_cast<volatile int*>(&drain_abort),
+                       p.status);
+        mbar_wait_warp(&empty_bar[i % STAGES], (i / STAGES) & 1u, reinterpret_cast<volatile int*>(&drain_abort),
+                       p.status);
+      }
+    } else if (warp == 1 && rank == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint32_t idesc = idesc_nvfp4(256, BN);
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t da0 = desc_kmajor_sw128(sbase);
+      const uint64_t db0 = desc_kmajor_sw128(sbase + Cfg::A_BYTES);
+      const uint32_t tsf0 = tmem_base + Cfg::SF_BASE;
+      constexpr uint32_t kStageUnits = Cfg::STAGE_BYTES >> 4;
+      uint32_t it = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = unit0; ok && tile < total; tile += unit_step) {
+        if (!mbar_wait_warp(&acce_bar, acc_phase ^ 1, &abort_flag, p.status)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < p.kblocks; kb += 2) {
+          const bool two = kb + 1 < p.kblocks;
+          const uint32_t st0 = it % STAGES, ph0 = (it / STAGES) & 1u;
+          const uint32_t st1 = (it + 1) % STAGES, ph1 = ((it + 1) / STAGES) & 1u;
+          if (!mbar_wait_warp(&sf_bar[st0], ph0, &abort_flag, p.status) ||
+              (two && !mbar_wait_warp(&sf_bar[st1], ph1, &abort_flag, p.status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (h == 1 && !two) break;
+              const uint32_t stage = h ? st1 : st0;
+              const int ks = min(4, (p.K - (kb + h) * 256) >> 6);
+              const uint64_t off = static_cast<uint64_t>(stage * kStageUnits);
+              const uint64_t da = da0 + off, db = db0 + off;
+              const uint32_t t_sfa = tsf0 + stage * Cfg::SF_COLS;
+              const uint32_t t_sfb = t_sfa + 16;
+#pragma unroll
+              for (int s = 0; s < 4; ++s) {
+                if (s < ks)
+                  umma_nvfp4_pair(tmem_base, da + 2 * s, db + 2 * s, idesc, t_sfa + 4 * s, t_sfb + (BN / 32) * s,
+                                  (kb + h > 0 || s > 0) ? 1u : 0u);
+              }
+              umma_commit_pair(&empty_bar[stage], 0x3);
+            }
+          }
+          __syncwarp();
+          it += two ? 2u : 1u;
+        }
+        if (!ok) break;
+        if (lane == 0) umma_commit_pair(&accf_bar, 0x3);
+        __syncwarp();
+        acc_phase ^= 1;
+      }
+      // wait until every MMA issued above has completed
+      if (lane == 0) umma_commit_pair(&done_bar, 0x1);
+      __syncwarp();
+      int drain_abort = 0;
+      mbar_wait_warp(&done_bar, 0, reinterpret_cast<volatile int*>(&drain_abort), p.status);
+    }
+  } else if (wg == 1) {
+    // ------------------------------------------------------------ scale writers
+    // as in gemm_nvfp4_kernel: warp q writes its TMEM lane quadrant; then one
+    // arrival per warp on CTA 0's scale-ready barrier of the stage
+    regs_dec();
+    const int q = warp & 3;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int tile = unit0; ok && tile < total; tile += unit_step) {
+      for (int kb = 0; kb < p.kblocks; ++kb) {
+        if (!mbar_wait(&full_bar[stage], phase, &abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sSFA = smem + stage * Cfg::STAGE_BYTES + Cfg::A_BYTES + Cfg::B_BYTES;
+        const uint8_t* sSFB = sSFA + Cfg::SFA_BYTES;
+        const uint32_t t_sf = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + Cfg::SF_BASE + stage * Cfg::SF_COLS;
+        uint32_t va[16];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const uint4 x = *reinterpret_cast<const uint4*>(sSFA + 512 * s + 16 * lane);
+          va[4 * s] = x.x;
+          va[4 * s + 1] = x.y;
+          va[4 * s + 2] = x.z;
+          va[4 * s + 3] = x.w;
+        }
+        tmem_st_32x32b_x16(t_sf, va);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t vb[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int col = 16 * h + 4 * i;
+            const int s = col / (BN / 32);
+            const int j = (col % (BN / 32)) / 4;
+            const uint4 x = *reinterpret_cast<const uint4*>(sSFB + j * 2048 + 512 * s + 16 * lane);
+            vb[4 * i] = x.x;
+            vb[4 * i + 1] = x.y;
+            vb[4 * i + 2] = x.z;
+            vb[4 * i + 3] = x.w;
+          }
+          tmem_st_32x32b_x16(t_sf + 16 + 16 * h, vb);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(mapa_shared(&sf_bar[stage], 0));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    regs_inc();
+    const int ew = warp - 8;
+    const int q = warp & 3;      // TMEM lane quadrant: output rows 32q ..
+    const int part = ew >> 2;    // column half: 128 part ..
+    uint8_t* stg = smem + STAGES * Cfg::STAGE_BYTES + ew * Cfg::EPI_WARP_BYTES;
+    const uint32_t acce_lead = mapa_shared(&acce_bar, 0);
+    const float alpha = __ldg(p.alpha);
+    uint32_t acc_phase = 0;
+    for (int tile = unit0; tile < total; tile += unit_step) {
+      const int mp = tile / p.n_tiles, nt = tile - mp * p.n_tiles;
+      const int mt = 2 * mp + static_cast<int>(rank);
+      if (!mbar_wait(&accf_bar, acc_phase, &abort_flag, p.status)) break;
+      tc_fence_after();
+      constexpr int COLS = BN / 2;
+      uint32_t r[COLS / 32][32];
+      drain<COLS>(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + part * COLS, r);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(acce_lead);
+      acc_phase ^= 1;
+      if (mt >= m_tiles) continue;  // rows past M (the second half of the last pair)
+      // row `lane` of a 32 x 64 box, 128-byte rows with the 128-byte swizzle
+      // (16-byte chunk j of row r at chunk j ^ (r % 8)); two boxes per tile
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        // this warp's previous box has been read out of the staging buffer
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        uint8_t* row = stg + lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t* v = r[2 * g + j / 4] + 8 * (j % 4);
+          uint4 o;
+          o.x = pack_bf16x2(__uint_as_float(v[0]) * alpha, __uint_as_float(v[1]) * alpha);
+          o.y = pack_bf16x2(__uint_as_float(v[2]) * alpha, __uint_as_float(v[3]) * alpha);
+          o.z = pack_bf16x2(__uint_as_float(v[4]) * alpha, __uint_as_float(v[5]) * alpha);
+          o.w = pack_bf16x2(__uint_as_float(v[6]) * alpha, __uint_as_float(v[7]) * alpha);
+          *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = o;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int x = nt * BN + part * COLS + 64 * g, y = mt * 128 + 32 * q;
+          if (x < p.N && y < p.M) tma_store_2d(&tmOut, stg, x, y);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) bulk_wait_all();  // this warp's stores are complete
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no MMA, copy or arrival of the pair touches this CTA after this point
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-using Dense1Cfg = GemmCfg<256, 1, 4, kEpiDense, 1>;
-using Dense2Cfg = GemmCfg<256, 1, 4, kEpiDense, 2>;
-using Dense4Cfg = GemmCfg<256, 1, 4, kEpiDense, 4>;
 using GatedCfg = GemmCfg<256, 1, 4, kEpiGatedQuant>;
 using AmaxCfg = GemmCfg<256, 1, 4, kEpiGatedAmax>;
 using DownCfg = GemmCfg<128, 2, 4, kEpiDownSum>;
@@ -585,47 +915,24 @@ static cudaError_t launch_cfg(const GemmMaps& maps, const GemmParams& p, int gri
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  if constexpr (Cfg::CL == 1) {
-    gemm_nvfp4_kernel<Cfg><<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(maps.a, maps.b, p);
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = Cfg::CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    // the persistent grid must fit in one wave of co-resident clusters
-    static int max_clusters = -1;
-    if (max_clusters < 0) {
-      cudaLaunchConfig_t q = {};
-      q.gridDim = dim3(Cfg::CL, 1, 1);
-      q.blockDim = dim3(kThreads, 1, 1);
-      q.dynamicSmemBytes = Cfg::SMEM_BYTES;
-      q.attrs = attr;
-      q.numAttrs = 1;
-      int n = 0;
-      max_clusters = (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_kernel<Cfg>, &q) == cudaSuccess) ? n : 0;
-    }
-    if (max_clusters > 0 && grid / Cfg::CL > max_clusters) grid = max_clusters * Cfg::CL;
-    cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel<Cfg>, maps.a, maps.b, p);
-    if (e != cudaSuccess) return e;
-  }
+  gemm_nvfp4_kernel<Cfg><<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(maps.a, maps.b, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream,
-                        int cluster) {
+cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {
   switch (mode) {
-    case kEpiDense:
-      if (cluster == 4) return launch_cfg<Dense4Cfg>(maps, p, grid, stream);
-      if (cluster == 2) return launch_cfg<Dense2Cfg>(maps, p, grid, stream);
-      return launch_cfg<Dense1Cfg>(maps, p, grid, stream);
+    case kEpiDense: {
+      static bool attr_set = false;
+      if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             PairCfg::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+      }
+      if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;  // whole CTA pairs
+      gemm_pair_kernel<<<grid, kThreads, PairCfg::SMEM_BYTES, stream>>>(maps.a, maps.b, maps.out, p);
+      return cudaGetLastError();
+    }
     case kEpiGatedQuant: return launch_cfg<GatedCfg>(maps, p, grid, stream);
     case kEpiGatedAmax: return launch_cfg<AmaxCfg>(maps, p, grid, stream);
     case kEpiDownSum: return launch_cfg<DownCfg>(maps, p, grid, stream);

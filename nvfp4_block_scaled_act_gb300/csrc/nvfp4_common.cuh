@@ -80,6 +80,42 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Non-blocking test of a phase's completion.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Warp-collective form of mbar_wait: every lane of a converged warp calls it and
+// all get the same answer, so the caller's loop state stays warp-uniform (the
+// addresses, coordinates and descriptors that one lane then hands to TMA or
+// tcgen05 instructions are computed by the whole warp).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                               int* status) {
+  const uint32_t a = smem_u32(bar);
+  if (__all_sync(0xFFFFFFFFu, mbar_test_wait(a, parity))) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (__all_sync(0xFFFFFFFFu, mbar_try_wait(a, parity))) return true;
+    if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) return false;
+    if (__any_sync(0xFFFFFFFFu, clock64() - t0 > kWaitLimitCycles)) {
+      if ((threadIdx.x & 31) == 0) {
+        *abort_flag = 1;
+        record_status(status, kStatusTimeout);
+      }
+      __syncwarp();
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------
@@ -102,26 +138,6 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(smem_dst)),
       "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Multicast variants: the data (and the complete_tx) land at the same
-// CTA-relative offsets in every CTA of the cluster named in `mask`.
-__device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ void bulk_load_mc(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
-                                             uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], "
-      "%4;" ::"r"(smem_u32(smem_dst)),
-      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
       : "memory");
 }
 
@@ -182,14 +198,72 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Arrive on the mbarrier at the same offset in every CTA named in `mask` once
-// every tcgen05 operation issued so far by this thread has completed.
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask) {
+// --- CTA pairs (cta_group::2) ------------------------------------------------
+// Every tcgen05 instruction of a kernel that uses pairs carries cta_group::2.
+// The pair's allocation is collective: warp 1 of both CTAs issues it and both
+// receive the same column address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Issued by CTA 0 of the pair: M = 256 rows, 128 of them in each CTA (A at the
+// same shared-memory offset in both), N rows of B split the same way (rows
+// [0, N/2) in CTA 0, the rest in CTA 1), D rows in each CTA's TMEM at d_tmem.
+// Each CTA's TMEM holds the scales of its own A rows and of all N B rows at the
+// given columns (the single-CTA layouts).
+__device__ __forceinline__ void umma_nvfp4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Arrive on the mbarrier at the same offset in every CTA of the pair named in
+// `mask` once every tcgen05 operation issued so far by this thread completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
           smem_u32(bar)),
       "h"(mask)
       : "memory");
+}
+
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(const void* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier given by its cluster address (possibly in the other
+// CTA of the pair), with the default CTA-scope release.  Callers publish only
+// work whose completion they have already waited for (tcgen05.wait::st or
+// ::ld, or a full barrier of their CTA's copies), so the arrival carries no
+// pending writes; a cluster-scope release costs a few hundred to a thousand
+// cycles per arrival and was the pair pipeline's bottleneck.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Store a 2D box from shared memory into the tensor of `map` (this thread's
+// bulk group).  Elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];\n\t"
+               "cp.async.bulk.commit_group;" ::"l"(map),
+               "r"(x), "r"(y), "r"(smem_u32(smem_src))
+               : "memory");
 }
 
 // Copy 32 rows x 16 bytes from shared memory into TMEM columns [taddr, taddr+4)

@@ -58,17 +58,19 @@ struct GemmParams {
 struct GemmMaps {
   CUtensorMap a;
   CUtensorMap b;
+  CUtensorMap out;  // dense mode: the bf16 output (boxes of 32 rows x 64 columns, 128-byte swizzle)
 };
 
 // Build a 2D TMA map over a [rows, row_bytes] byte matrix, box box_rows x 128
 // bytes, 128-byte swizzle.
 bool make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows = 128);
 
-// `cluster` (dense mode only): CTAs per cluster sharing each B tile through
-// TMA multicast (1, 2 or 4); the grid must be a multiple of it.  The B map's
-// box holds 128 rows for cluster 1 and 2 and 64 rows for cluster 4 (one box
-// per CTA and 128-row block).
-cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream,
-                        int cluster = 1);
+// Build the TMA map of a [rows, cols] bf16 output with a row pitch of ld
+// elements: boxes of 32 rows x 64 columns, 128-byte swizzle (TMA stores).
+bool make_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t ld);
+
+// B boxes are 128 rows in every mode.  The dense mode runs on CTA pairs (the
+// grid counts CTAs and must be even: one pair per 256 x 256 output tile).
+cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream);
 
 }  // namespace nvfp4
