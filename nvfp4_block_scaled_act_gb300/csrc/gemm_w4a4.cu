@@ -727,61 +727,82 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_wait_warp(&empty_bar[i % STAGES], (i / STAGES) & 1u, reinterpret_cast<volatile int*>(&drain_abort),
                        p.status);
       }
-    } else if (warp == 1 && rank == 0) {
+    } else if (warp == 1 && rank == 0 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
+      // One lane, and as little work between MMAs as possible: the tensor pipe
+      // queues only a few MMAs, so every cycle the lane spends on waits and
+      // bookkeeping beyond that is idle pipe.  Two stages per pass share one
+      // wait (the writers complete stages in order, so the second stage's
+      // scale-ready phase implies the first's); stage, phase and operand
+      // addresses advance incrementally.
       const uint32_t idesc = idesc_nvfp4(256, BN);
       const uint32_t sbase = smem_u32(smem);
       const uint64_t da0 = desc_kmajor_sw128(sbase);
       const uint64_t db0 = desc_kmajor_sw128(sbase + Cfg::A_BYTES);
       const uint32_t tsf0 = tmem_base + Cfg::SF_BASE;
       constexpr uint32_t kStageUnits = Cfg::STAGE_BYTES >> 4;
-      uint32_t it = 0, acc_phase = 0;
+      const bool kfull = (p.K & 255) == 0;
+      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      uint64_t da = da0, db = db0;
+      uint32_t t_sfa = tsf0;
+      auto advance = [&]() {
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+          da = da0;
+          db = db0;
+          t_sfa = tsf0;
+        } else {
+          da += kStageUnits;
+          db += kStageUnits;
+          t_sfa += Cfg::SF_COLS;
+        }
+      };
+      auto issue_stage = [&](int kb) {
+        const uint32_t t_sfb = t_sfa + 16;
+        if (kfull || (p.K - kb * 256) >= 256) {
+          umma_nvfp4_pair(tmem_base, da, db, idesc, t_sfa, t_sfb, kb > 0 ? 1u : 0u);
+#pragma unroll
+          for (int s = 1; s < 4; ++s)
+            umma_nvfp4_pair(tmem_base, da + 2 * s, db + 2 * s, idesc, t_sfa + 4 * s, t_sfb + (BN / 32) * s, 1u);
+        } else {
+          const int ks = (p.K - kb * 256) >> 6;
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            if (s < ks)
+              umma_nvfp4_pair(tmem_base, da + 2 * s, db + 2 * s, idesc, t_sfa + 4 * s, t_sfb + (BN / 32) * s,
+                              (kb > 0 || s > 0) ? 1u : 0u);
+        }
+        umma_commit_pair(&empty_bar[stage], 0x3);
+      };
       bool ok = true;
       for (int tile = unit0; ok && tile < total; tile += unit_step) {
-        if (!mbar_wait_warp(&acce_bar, acc_phase ^ 1, &abort_flag, p.status)) break;
+        if (!mbar_wait(&acce_bar, acc_phase ^ 1, &abort_flag, p.status)) break;
         tc_fence_after();
         for (int kb = 0; kb < p.kblocks; kb += 2) {
           const bool two = kb + 1 < p.kblocks;
-          const uint32_t st0 = it % STAGES, ph0 = (it / STAGES) & 1u;
-          const uint32_t st1 = (it + 1) % STAGES, ph1 = ((it + 1) / STAGES) & 1u;
-          if (!mbar_wait_warp(&sf_bar[st0], ph0, &abort_flag, p.status) ||
-              (two && !mbar_wait_warp(&sf_bar[st1], ph1, &abort_flag, p.status))) {
+          const uint32_t wst = two ? (stage + 1 == STAGES ? 0u : stage + 1) : stage;
+          const uint32_t wph = (two && stage + 1 == STAGES) ? phase ^ 1 : phase;
+          if (!mbar_wait(&sf_bar[wst], wph, &abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (lane == 0) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if (h == 1 && !two) break;
-              const uint32_t stage = h ? st1 : st0;
-              const int ks = min(4, (p.K - (kb + h) * 256) >> 6);
-              const uint64_t off = static_cast<uint64_t>(stage * kStageUnits);
-              const uint64_t da = da0 + off, db = db0 + off;
-              const uint32_t t_sfa = tsf0 + stage * Cfg::SF_COLS;
-              const uint32_t t_sfb = t_sfa + 16;
-#pragma unroll
-              for (int s = 0; s < 4; ++s) {
-                if (s < ks)
-                  umma_nvfp4_pair(tmem_base, da + 2 * s, db + 2 * s, idesc, t_sfa + 4 * s, t_sfb + (BN / 32) * s,
-                                  (kb + h > 0 || s > 0) ? 1u : 0u);
-              }
-              umma_commit_pair(&empty_bar[stage], 0x3);
-            }
+          issue_stage(kb);
+          advance();
+          if (two) {
+            issue_stage(kb + 1);
+            advance();
           }
-          __syncwarp();
-          it += two ? 2u : 1u;
         }
         if (!ok) break;
-        if (lane == 0) umma_commit_pair(&accf_bar, 0x3);
-        __syncwarp();
+        umma_commit_pair(&accf_bar, 0x3);
         acc_phase ^= 1;
       }
       // wait until every MMA issued above has completed
-      if (lane == 0) umma_commit_pair(&done_bar, 0x1);
-      __syncwarp();
+      umma_commit_pair(&done_bar, 0x1);
       int drain_abort = 0;
-      mbar_wait_warp(&done_bar, 0, reinterpret_cast<volatile int*>(&drain_abort), p.status);
+      mbar_wait(&done_bar, 0, reinterpret_cast<volatile int*>(&drain_abort), p.status);
     }
   } else if (wg == 1) {
     // ------------------------------------------------------------ scale writers

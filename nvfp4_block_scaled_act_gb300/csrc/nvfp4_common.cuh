@@ -61,25 +61,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete.  Returns false, and
-// raises the CTA's abort flag and the device status word, if it takes longer
-// than kWaitLimitCycles or if another role of the CTA has already aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_try_wait(a, parity)) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
-      *abort_flag = 1;
-      record_status(status, kStatusTimeout);
-      return false;
-    }
-  }
-}
-
 // Non-blocking test of a phase's completion.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -91,6 +72,25 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Returns false, and
+// raises the CTA's abort flag and the device status word, if it takes longer
+// than kWaitLimitCycles or if another role of the CTA has already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_test_wait(a, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      *abort_flag = 1;
+      record_status(status, kStatusTimeout);
+      return false;
+    }
+  }
 }
 
 // Warp-collective form of mbar_wait: every lane of a converged warp calls it and
