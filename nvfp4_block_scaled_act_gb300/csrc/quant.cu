@@ -2,25 +2,25 @@
 // on nvfp4 activations on sm_120", section "Changes"; the global g = 448 * 6 /
 // amax of "Add BF16_FP4 GEMM ... for W4A16 workloads", section "API").
 //
-// quant_act: HBM-bound.  One warp handles a 256-element chunk of a row: each
-// lane loads 8 bf16 with one 16-byte load, two lanes form a 16-element block
-// and exchange their partial amax with a warp shuffle, both derive the same
-// E4M3 scale, each converts its 8 values to e2m1 with the hardware cvt and
-// stores 4 code bytes; the even lane stores the scale byte at its swizzled
-// position.  Rows are split into chunks, so long rows spread over many warps.
+// quant_act: HBM-bound.  Each lane owns one 16-element block: two 16-byte
+// loads, the block amax on packed bf16 magnitudes, one E4M3 scale, sixteen
+// conversions to e2m1 (hardware cvt), one 8-byte code store and the scale byte
+// at its swizzled position.  A warp covers 512 consecutive elements of a row
+// (1 KB, coalesced); rows are split into such chunks, so long rows spread over
+// many warps.  (Two lanes per block computed every per-block step twice.)
 #include "nvfp4_common.cuh"
 #include "nvfp4_internal.h"
 
 namespace nvfp4 {
 
-constexpr int kQuantUnroll = 4;  // chunks per warp and iteration, loads issued together
+constexpr int kQuantUnroll = 2;  // 512-element chunks per warp and iteration, loads issued together
 
-// Work item = kQuantUnroll consecutive 256-element chunks of one row (padded
+// Work item = kQuantUnroll consecutive 512-element chunks of one row (padded
 // rows and columns included), so one 32-bit division per item finds its row.
 // The grid is persistent; each warp loads its next item while it converts
 // the current one.
 struct QuantItem {
-  uint4 raw[kQuantUnroll];
+  uint4 raw[kQuantUnroll][2];
 };
 
 __device__ __forceinline__ void quant_load_item(QuantItem& it, uint32_t item, uint32_t total, uint32_t groups,
@@ -32,11 +32,11 @@ __device__ __forceinline__ void quant_load_item(QuantItem& it, uint32_t item, ui
   const uint16_t* xrow = x + static_cast<int64_t>(r32) * ldx;
 #pragma unroll
   for (int u = 0; u < kQuantUnroll; ++u) {
-    const uint32_t ch = ch0 + u;
-    const int64_t cc = static_cast<int64_t>(ch) * 16 + (lane >> 1);
-    it.raw[u] = (row_real && ch < chunks && cc < C)
-                    ? __ldg(reinterpret_cast<const uint4*>(xrow + static_cast<int64_t>(ch) * 256 + lane * 8))
-                    : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t cc = (ch0 + u) * 32 + lane;  // this lane's block
+    const bool in = row_real && ch0 + u < chunks && cc < C;
+    const uint4* src = reinterpret_cast<const uint4*>(xrow + static_cast<int64_t>(cc) * 16);
+    it.raw[u][0] = in ? __ldg(src) : make_uint4(0u, 0u, 0u, 0u);
+    it.raw[u][1] = in ? __ldg(src + 1) : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -69,8 +69,8 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restri
   }
   __syncthreads();
   const int lane = threadIdx.x & 31;
-  const uint32_t chunks = static_cast<uint32_t>((Cp * 16 + 255) / 256);  // per row
-  const uint32_t groups = (chunks + kQuantUnroll - 1) / kQuantUnroll;   // per row
+  const uint32_t chunks = static_cast<uint32_t>((Cp + 31) / 32);       // 512-element chunks per row
+  const uint32_t groups = (chunks + kQuantUnroll - 1) / kQuantUnroll;  // items per row
   const uint32_t total = static_cast<uint32_t>(Mp) * groups;
   const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
   const int64_t cpad4 = Cp / 4;
@@ -88,36 +88,42 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restri
     uint8_t* srow = scales + ((r >> 7) * cpad4) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      const uint32_t ch = ch0 + u;
-      if (ch >= chunks) break;  // warp-uniform
-      const uint32_t cc = ch * 16 + (lane >> 1);  // scale column of this lane's block
+      if (ch0 + u >= chunks) break;  // warp-uniform
+      const uint32_t cc = (ch0 + u) * 32 + lane;  // scale column of this lane's block
       const bool real = row_real && cc < C;
-      const uint32_t w[4] = {cur.raw[u].x, cur.raw[u].y, cur.raw[u].z, cur.raw[u].w};
+      const uint32_t w[8] = {cur.raw[u][0].x, cur.raw[u][0].y, cur.raw[u][0].z, cur.raw[u][0].w,
+                             cur.raw[u][1].x, cur.raw[u][1].y, cur.raw[u][1].z, cur.raw[u][1].w};
       // block amax on packed bf16 magnitudes (the max of bf16 values is exact;
       // like fmaxf, __hmax2 returns the other operand when one is NaN)
-      const uint32_t m0 = w[0] & 0x7FFF7FFFu, m1 = w[1] & 0x7FFF7FFFu;
-      const uint32_t m2 = w[2] & 0x7FFF7FFFu, m3 = w[3] & 0x7FFF7FFFu;
-      const __nv_bfloat162 x01 = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&m0),
-                                         *reinterpret_cast<const __nv_bfloat162*>(&m1));
-      const __nv_bfloat162 x23 = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&m2),
-                                         *reinterpret_cast<const __nv_bfloat162*>(&m3));
-      const __nv_bfloat162 xm = __hmax2(x01, x23);
+      __nv_bfloat162 m[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t a = w[j] & 0x7FFF7FFFu;
+        m[j] = *reinterpret_cast<const __nv_bfloat162*>(&a);
+      }
+      const __nv_bfloat162 xm =
+          __hmax2(__hmax2(__hmax2(m[0], m[1]), __hmax2(m[2], m[3])), __hmax2(__hmax2(m[4], m[5]), __hmax2(m[6], m[7])));
       const uint32_t a01 = *reinterpret_cast<const uint32_t*>(&xm);
-      float amax = fmaxf(bf16_bits_to_f32(a01 & 0xFFFFu), bf16_bits_to_f32(a01 >> 16));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      const float amax = fmaxf(bf16_bits_to_f32(a01 & 0xFFFFu), bf16_bits_to_f32(a01 >> 16));
       const uint32_t s8 = f32_to_e4m3(__fmul_rn(__fdiv_rn(amax, 6.0f), g));
       const float rr = r_of_s8[s8];
       if (real) {
-        float v[8];
+        uint32_t packed[2] = {0u, 0u};
+        if (rr != 0.0f) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          v[2 * j] = bf16_bits_to_f32(w[j] & 0xFFFFu);
-          v[2 * j + 1] = bf16_bits_to_f32(w[j] >> 16);
+          for (int h = 0; h < 2; ++h) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              v[2 * j] = bf16_bits_to_f32(w[4 * h + j] & 0xFFFFu);
+              v[2 * j + 1] = bf16_bits_to_f32(w[4 * h + j] >> 16);
+            }
+            packed[h] = f32x8_to_e2m1x8(v, rr);
+          }
         }
-        const uint32_t packed = (rr != 0.0f) ? f32x8_to_e2m1x8(v, rr) : 0u;
-        *reinterpret_cast<uint32_t*>(crow + ch * 128 + lane * 4) = packed;
+        *reinterpret_cast<uint2*>(crow + static_cast<int64_t>(cc) * 8) = make_uint2(packed[0], packed[1]);
       }
-      if ((lane & 1) == 0 && cc < Cp) srow[(cc >> 2) * 512 + (cc & 3)] = real ? static_cast<uint8_t>(s8) : 0;
+      if (cc < Cp) srow[(cc >> 2) * 512 + (cc & 3)] = real ? static_cast<uint8_t>(s8) : 0;
     }
     cur = nxt;
   }
@@ -191,7 +197,7 @@ __global__ void __launch_bounds__(256) reduce_max_kernel(const float* __restrict
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, const float* d_global,
                              uint8_t* codes, uint8_t* scales, int num_sms, cudaStream_t stream) {
   const int64_t C = K / 16, Cp = (C + 3) / 4 * 4, Mp = (M + 127) / 128 * 128;
-  const int64_t chunks = (Cp * 16 + 255) / 256;
+  const int64_t chunks = (Cp + 31) / 32;
   const int64_t items = Mp * ((chunks + kQuantUnroll - 1) / kQuantUnroll);  // warp work items
   if (items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   // persistent: 4 blocks of 8 warps per SM (the register limit at 256 threads)
