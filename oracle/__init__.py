@@ -54,6 +54,8 @@ _SIGS = {
     "nvo_moe_w4a4": (None, [_P, _I64, _I64, _I64, _I64, _I64, _P, _P, _F, _P, _P, _P,
                              _F, _P, _P, _P, _P, _P, _P]),
     "nvo_moe_h_amax": (None, [_P, _I64, _I64, _I64, _I64, _F, _P, _P, _P, _P]),
+    "nvo_moe_w4a16": (None, [_P, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P,
+                              _P, _P]),
 }
 
 
@@ -231,6 +233,25 @@ def moe_w4a4(x, topk_ids, topk_w, g_a1, w13_codes, w13_sf, alpha13, g_a2, w2_cod
                        _ptr(out), _ptr(hc) if want_h else None, _ptr(hs) if want_h else None)
     out = out.view(torch.bfloat16)
     return (out, hc, hs) if want_h else out
+
+
+def moe_w4a16(x, topk_ids, topk_w, w13_codes, w13_sf, alpha13, w2_codes, w2_sf, alpha2, E, H, I,
+              want_h: bool = False):
+    """W4A16 MoE layer (bf16 activations throughout): bf16 [T, H] -> bf16 [T, H];
+    optionally the bf16 intermediate h [T * topk, I] (row t * topk + slot)."""
+    T, topk = topk_ids.shape
+    u = _u16(x)
+    ids = topk_ids.to(torch.int32).contiguous()
+    w = topk_w.to(torch.float32).contiguous()
+    a13 = torch.as_tensor(alpha13, dtype=torch.float32).contiguous()
+    a2 = torch.as_tensor(alpha2, dtype=torch.float32).contiguous()
+    out = _bf16_out((T, H))
+    h = _bf16_out((T * topk, I)) if want_h else None
+    lib().nvo_moe_w4a16(_ptr(u), T, H, I, E, topk, _ptr(ids), _ptr(w), _ptr(w13_codes.contiguous()),
+                        _ptr(w13_sf.contiguous()), _ptr(a13), _ptr(w2_codes.contiguous()),
+                        _ptr(w2_sf.contiguous()), _ptr(a2), _ptr(out), _ptr(h) if want_h else None)
+    out = out.view(torch.bfloat16)
+    return (out, h.view(torch.bfloat16)) if want_h else out
 
 
 def moe_h_amax(x_calib, g_a1, w13_codes, w13_sf, alpha13, E, H, I) -> torch.Tensor:

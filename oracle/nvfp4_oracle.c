@@ -473,6 +473,77 @@ void nvo_moe_w4a4(const uint16_t* x, int64_t T, int64_t H, int64_t I, int64_t E,
 }
 
 /* ------------------------------------------------------------------------- */
+/* W4A16 MoE for small batches ([moe] "Changes": prefill runs W4A4 from 4     */
+/* tokens per expert and W4A16 below; "Decode ... and W4A16 prefill are       */
+/* untouched").  READING: [moe]'s layer with the activations never quantised   */
+/* (the W4A16 linear of [mmbf16] applied per expert):                          */
+/*   G = sum_k x[t,k] W13^[j,k],  U = sum_k x[t,k] W13^[I+j,k]   fp32, asc. k   */
+/*   h[j] = bf16(silu(alpha13[e] * G) * (alpha13[e] * U))   the intermediate is */
+/*          an activation of a W4A16 layer, so it is rounded to bf16            */
+/*   d[n] = alpha2[e] * sum_k h[k] W2^[n,k]                  fp32, asc. k       */
+/*   y[t,n] = sum over slots s in order of w[t,s] * d[n] (fp32), out = bf16(y)  */
+/* alpha13[e] = 1 / g13[e], alpha2[e] = 1 / g2[e].  Routes with an id outside  */
+/* [0, E) are dropped.                                                          */
+/* ------------------------------------------------------------------------- */
+
+void nvo_moe_w4a16(const uint16_t* x, int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk,
+                   const int32_t* topk_ids, const float* topk_w, const uint8_t* w13_codes,
+                   const uint8_t* w13_sf, const float* alpha13, const uint8_t* w2_codes,
+                   const uint8_t* w2_sf, const float* alpha2, uint16_t* out, uint16_t* h_out) {
+  const int64_t R = T * topk;
+  float* D = (float*)calloc((size_t)(R * H + 1), sizeof(float)); /* d per route */
+  float* W13 = (float*)malloc(sizeof(float) * (size_t)(2 * I * H + 1));
+  float* W2 = (float*)malloc(sizeof(float) * (size_t)(H * I + 1));
+  const size_t w13_bytes = (size_t)(2 * I) * (size_t)(H / 2), w13_sfb = nvo_scale_bytes(2 * I, H);
+  const size_t w2_bytes = (size_t)H * (size_t)(I / 2), w2_sfb = nvo_scale_bytes(H, I);
+  int64_t* routes = (int64_t*)malloc(sizeof(int64_t) * (size_t)(R + 1));
+
+  for (int64_t e = 0; e < E; ++e) {
+    int64_t nr = 0;
+    for (int64_t i = 0; i < R; ++i)
+      if (topk_ids[i] == e) routes[nr++] = i;
+    if (nr == 0) continue;
+    nvo_dequant(w13_codes + (size_t)e * w13_bytes, w13_sf + (size_t)e * w13_sfb, 2 * I, H, W13);
+    nvo_dequant(w2_codes + (size_t)e * w2_bytes, w2_sf + (size_t)e * w2_sfb, H, I, W2);
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t q = 0; q < nr; ++q) {
+      int64_t i = routes[q], t = i / topk;
+      float* h = (float*)malloc(sizeof(float) * (size_t)I);
+      for (int64_t j = 0; j < I; ++j) {
+        float G = 0.0f, U = 0.0f;
+        for (int64_t k = 0; k < H; ++k) G += nvo_bf16_to_f32(x[t * H + k]) * W13[j * H + k];
+        for (int64_t k = 0; k < H; ++k) U += nvo_bf16_to_f32(x[t * H + k]) * W13[(I + j) * H + k];
+        const uint16_t hb = nvo_f32_to_bf16(silu_f32(alpha13[e] * G) * (alpha13[e] * U));
+        if (h_out) h_out[i * I + j] = hb;
+        h[j] = nvo_bf16_to_f32(hb);
+      }
+      for (int64_t n = 0; n < H; ++n) {
+        float acc = 0.0f;
+        for (int64_t k = 0; k < I; ++k) acc += h[k] * W2[n * I + k];
+        D[i * H + n] = alpha2[e] * acc;
+      }
+      free(h);
+    }
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t n = 0; n < H; ++n) {
+      float y = 0.0f;
+      for (int64_t s = 0; s < topk; ++s) {
+        int64_t i = t * topk + s;
+        int32_t e = topk_ids[i];
+        if (e < 0 || e >= E) continue;
+        y += topk_w[i] * D[i * H + n];
+      }
+      out[t * H + n] = nvo_f32_to_bf16(y);
+    }
+  free(routes);
+  free(W13);
+  free(W2);
+  free(D);
+}
+
+/* ------------------------------------------------------------------------- */
 /* MoE calibration of the second GEMM's input ([moe] "Static activation        */
 /* scales": the largest per-expert input global feeds each GEMM).  READING:   */
 /* every calibration row goes through every expert (steps 1-3 above), so each  */

@@ -491,3 +491,90 @@ def test_moe_h_amax_is_max_over_rows_and_columns():
         a13 = np.float64(np.float32(d["a13"][e]))
         h = _silu64(a13 * (X @ W13[:I].T)) * (a13 * (X @ W13[I:].T))
         assert math.isclose(float(d["amax"][e]), float(np.abs(h).max()), rel_tol=1e-5)
+
+
+# ---------------------------------------------------------------------------
+# W4A16 MoE (bf16 activations, bf16 intermediate)
+# ---------------------------------------------------------------------------
+
+def _tiny_moe_w4a16(E=3, H=64, I=32, T=6, topk=2, seed=0, same_experts=False):
+    case = synthdata.moe_case(T, E, H, I, topk, seed=seed)
+    w13 = [case.w13(0 if same_experts else e) for e in range(E)]
+    w2 = [case.w2(0 if same_experts else e) for e in range(E)]
+    g13 = [oracle.global_scale(w) for w in w13]
+    g2 = [oracle.global_scale(w) for w in w2]
+    q13 = [oracle.quantize(w, g) for w, g in zip(w13, g13)]
+    q2 = [oracle.quantize(w, g) for w, g in zip(w2, g2)]
+    return dict(case=case, w13c=torch.cat([q[0] for q in q13]), w13s=torch.cat([q[1] for q in q13]),
+                w2c=torch.cat([q[0] for q in q2]), w2s=torch.cat([q[1] for q in q2]),
+                q13=q13, q2=q2, a13=[oracle.alpha_w4a16(g) for g in g13], a2=[oracle.alpha_w4a16(g) for g in g2],
+                E=E, H=H, I=I)
+
+
+def _w4a16_moe_fp64(d, x, ids, w):
+    """Brute force: fp64 sums of bf16 x against dequantised weights; h rounded
+    to bf16 with torch's conversion; gate = rows [0, I) of W13."""
+    E, H, I = d["E"], d["H"], d["I"]
+    X = x.to(torch.float64).numpy()
+    T, topk = ids.shape
+    y = np.zeros((T, H))
+    hs = np.zeros((T * topk, I))
+    for t in range(T):
+        for s in range(topk):
+            e = int(ids[t, s])
+            if e < 0 or e >= E:
+                continue
+            W13 = dequant_np(*d["q13"][e], 2 * I, H)
+            W2 = dequant_np(*d["q2"][e], H, I)
+            a13 = np.float64(np.float32(d["a13"][e]))
+            G = X[t] @ W13[:I].T
+            U = X[t] @ W13[I:].T
+            h = torch.from_numpy(_silu64(a13 * G) * (a13 * U)).to(torch.bfloat16).to(torch.float64).numpy()
+            hs[t * topk + s] = h
+            y[t] += float(w[t, s]) * np.float64(np.float32(d["a2"][e])) * (h @ W2.T)
+    return y, hs
+
+
+def test_moe_w4a16_reduces_to_gated_mlp():
+    """topk = 1 with weight 1: down(bf16(silu(gate) * up)) of one expert."""
+    d = _tiny_moe_w4a16(E=2, T=5, topk=1, seed=3)
+    case, E, H, I = d["case"], d["E"], d["H"], d["I"]
+    ids = torch.tensor([[1], [0], [1], [1], [0]], dtype=torch.int32)
+    w = torch.ones(5, 1)
+    out, h = oracle.moe_w4a16(case.x, ids, w, d["w13c"], d["w13s"], d["a13"], d["w2c"], d["w2s"], d["a2"],
+                              E, H, I, want_h=True)
+    ref, href = _w4a16_moe_fp64(d, case.x, ids, w)
+    out, h = bf16_np(out), bf16_np(h)
+    # h: the fp32 sums may round to the other side of a bf16 tie at most
+    assert np.all(np.abs(h - href) <= bf16_ulp(np.abs(href)) + 1e-30)
+    assert np.all(np.abs(out - ref) <= 2 * bf16_ulp(np.abs(ref).max(axis=1, keepdims=True)))
+
+
+def test_moe_w4a16_topk_weighted_sum():
+    d = _tiny_moe_w4a16(E=4, T=6, topk=3, seed=8, H=128, I=64)
+    case, E, H, I = d["case"], d["E"], d["H"], d["I"]
+    out = bf16_np(oracle.moe_w4a16(case.x, case.topk_ids, case.topk_w, d["w13c"], d["w13s"], d["a13"],
+                                   d["w2c"], d["w2s"], d["a2"], E, H, I))
+    ref, _ = _w4a16_moe_fp64(d, case.x, case.topk_ids, case.topk_w)
+    assert np.all(np.abs(out - ref) <= 2 * bf16_ulp(np.abs(ref).max(axis=1, keepdims=True)))
+
+
+def test_moe_w4a16_invalid_ids_contribute_nothing():
+    d = _tiny_moe_w4a16(E=3, T=4, topk=2, seed=6)
+    case, E, H, I = d["case"], d["E"], d["H"], d["I"]
+    args = (d["w13c"], d["w13s"], d["a13"], d["w2c"], d["w2s"], d["a2"], E, H, I)
+    ids = case.topk_ids.clone()
+    ids[:, 1] = -1
+    a = oracle.moe_w4a16(case.x, ids, case.topk_w, *args)
+    b = oracle.moe_w4a16(case.x, case.topk_ids[:, :1].contiguous(), case.topk_w[:, :1].contiguous(), *args)
+    assert torch.equal(a, b)
+
+
+def test_moe_w4a16_identical_experts_ignore_routing():
+    d = _tiny_moe_w4a16(E=4, T=6, topk=3, seed=5, same_experts=True)
+    case, E, H, I = d["case"], d["E"], d["H"], d["I"]
+    args = (d["w13c"], d["w13s"], d["a13"], d["w2c"], d["w2s"], d["a2"], E, H, I)
+    w = case.topk_w
+    out = bf16_np(oracle.moe_w4a16(case.x, case.topk_ids, w, *args))
+    one = bf16_np(oracle.moe_w4a16(case.x, torch.zeros(6, 1, dtype=torch.int32), w.sum(1, keepdim=True), *args))
+    assert np.all(np.abs(out - one) <= 2 * bf16_ulp(np.abs(one).max(axis=1, keepdims=True)))
