@@ -219,6 +219,35 @@ nvfp4_status nvfp4_moe_calibrate(const void* x_calib_bf16, int64_t Tc, int64_t H
                                  float* d_g_a2, void* workspace, size_t ws_bytes,
                                  nvfp4_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * W4A16 MoE for small batches: decode and prefills with few tokens per expert
+ * (the W4A4 MoE prefill page, section "Changes", keeps W4A16 below 4 tokens
+ * per expert).  Same weight banks as nvfp4_moe_w4a4, no repack; activations
+ * are never quantised:
+ *   G, U = x @ W13[e][0:I].T, x @ W13[e][I:2I].T          (fp32 accumulation)
+ *   h    = bf16(silu(alpha13[e] * G) * (alpha13[e] * U))
+ *   out  = bf16(sum over the token's slots, in slot order, of
+ *               w * alpha2[e] * (h @ W2[e].T))              (fp32 sum)
+ * with d_alpha13[e] = 1 / g_w13[e] and d_alpha2[e] = 1 / g_w2[e] (no
+ * activation global).  x: bf16 [T, H], contiguous, 16-byte aligned.  Routes
+ * and weights as nvfp4_moe_w4a4; ids outside [0, E) set
+ * NVFP4_ERR_BAD_EXPERT_ID in the device word and are dropped.
+ * Shapes: 1 <= T <= 64, 1 <= topk <= 8, H % 128 == 0, I % 128 == 0,
+ * E <= 1024; T = 0 returns NVFP4_OK with no launch.  The result is
+ * deterministic (no atomics in the sums).
+ * --------------------------------------------------------------------------- */
+
+/* Workspace bytes of nvfp4_moe_w4a16 for T tokens. */
+size_t nvfp4_moe_w4a16_workspace(int64_t T, int64_t H, int64_t I, int64_t E, int topk);
+
+/* route -> gate_up (SiLU * up, bf16 h) -> down (routing weight) -> slot sum
+ * -> bf16.  No host synchronisation. */
+nvfp4_status nvfp4_moe_w4a16(const void* x_bf16, int64_t T, int64_t H, int64_t I, int64_t E, int topk,
+                             const int32_t* topk_ids, const float* topk_w, const uint8_t* w13_codes,
+                             const uint8_t* w13_sf, const float* d_alpha13, const uint8_t* w2_codes,
+                             const uint8_t* w2_sf, const float* d_alpha2, void* out_bf16, void* workspace,
+                             size_t ws_bytes, nvfp4_stream_t stream);
+
 /* Layout of the MoE workspace, for inspection of the intermediate stages
  * (all offsets in bytes from the workspace pointer, 256-byte aligned).  The
  * composite call fills:

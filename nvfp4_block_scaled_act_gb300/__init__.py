@@ -65,6 +65,9 @@ SIGNATURES = {
     "nvfp4_moe_w4a4": (_ST, [_P, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                              _P, _P, _P, _SZ, _P]),
     "nvfp4_moe_calibrate": (_ST, [_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "nvfp4_moe_w4a16_workspace": (_SZ, [_I64, _I64, _I64, _I64, _I]),
+    "nvfp4_moe_w4a16": (_ST, [_P, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                              _P]),
     "nvfp4_device_status": (_ST, [_P, ctypes.POINTER(ctypes.c_int32)]),
 }
 
@@ -221,6 +224,29 @@ def nvfp4_moe_w4a4(x, topk_ids, topk_w, g_a1, w13_codes, w13_sf, alpha13, g_a2, 
         _ptr(x), T, H, I, E, topk, _ptr(topk_ids), _ptr(topk_w), _ptr(g_a1), _ptr(w13_codes),
         _ptr(w13_sf), _ptr(alpha13), _ptr(g_a2), _ptr(w2_codes), _ptr(w2_sf), _ptr(alpha2),
         _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def nvfp4_moe_w4a16_workspace(T: int, H: int, I: int, E: int, topk: int) -> int:
+    return int(load_library().nvfp4_moe_w4a16_workspace(T, H, I, E, topk))
+
+
+def nvfp4_moe_w4a16(x, topk_ids, topk_w, w13_codes, w13_sf, alpha13, w2_codes, w2_sf, alpha2, E: int, I: int,
+                    out=None, workspace=None, stream=None):
+    """W4A16 MoE layer for small batches (T <= 64): bf16 [T, H] -> bf16 [T, H];
+    alpha13 = 1 / g_w13 and alpha2 = 1 / g_w2 per expert."""
+    _cuda(x, "x")
+    T, H = x.shape
+    topk = topk_ids.shape[1]
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(max(nvfp4_moe_w4a16_workspace(T, H, I, E, topk), 1), dtype=torch.uint8,
+                                device=x.device)
+    _check("nvfp4_moe_w4a16", load_library().nvfp4_moe_w4a16(
+        _ptr(x), T, H, I, E, topk, _ptr(topk_ids), _ptr(topk_w), _ptr(w13_codes), _ptr(w13_sf),
+        _ptr(alpha13), _ptr(w2_codes), _ptr(w2_sf), _ptr(alpha2), _ptr(out), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
     return out
 
 

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnvfp4.so")
-SOURCES = ["api.cu", "quant.cu", "gemm_w4a4.cu", "gemv_w4a16.cu", "moe.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm_w4a4.cu", "gemv_w4a16.cu", "moe.cu", "moe_w4a16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -421,6 +421,96 @@ nvfp4_status nvfp4_moe_w4a4(const void* x, int64_t T, int64_t H, int64_t I, int6
   return cuda_status(launch_moe_finalize(w.y, T * H, out, dev->sms, stream));
 }
 
+namespace {
+struct MoeW16Layout {
+  size_t n_slots, slot_expert, slot_start, slot_count, route_list, tok_shift, h_amax, h, partial, total;
+};
+MoeW16Layout moe_w16_layout(int64_t T, int64_t H, int64_t I, int64_t E, int topk) {
+  MoeW16Layout L{};
+  const int64_t R = T * topk;
+  const int64_t S = R < E ? R : E;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  L.n_slots = take(sizeof(int32_t));
+  L.slot_expert = take(static_cast<size_t>(S) * sizeof(int32_t));
+  L.slot_start = take(static_cast<size_t>(S) * sizeof(int32_t));
+  L.slot_count = take(static_cast<size_t>(S) * sizeof(int32_t));
+  L.route_list = take(static_cast<size_t>(R) * sizeof(int32_t));
+  L.tok_shift = take(static_cast<size_t>(T) * sizeof(int32_t));
+  L.h_amax = take(static_cast<size_t>(R) * sizeof(uint32_t));
+  L.h = take(static_cast<size_t>(R * I) * sizeof(uint16_t));
+  L.partial = take(static_cast<size_t>(R * H) * sizeof(float));
+  L.total = off;
+  return L;
+}
+nvfp4_status moe_w16_check(int64_t T, int64_t H, int64_t I, int64_t E, int topk) {
+  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (T > 64 || topk > 8 || H % 128 != 0 || I % 128 != 0 || E > 1024) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (H > (1 << 16) || I > (1 << 16) || E * 2 * I > (1LL << 30) || E * H > (1LL << 30))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return NVFP4_OK;
+}
+}  // namespace
+
+size_t nvfp4_moe_w4a16_workspace(int64_t T, int64_t H, int64_t I, int64_t E, int topk) {
+  if (moe_w16_check(T, H, I, E, topk) != NVFP4_OK) return 0;
+  return moe_w16_layout(T, H, I, E, topk).total;
+}
+
+nvfp4_status nvfp4_moe_w4a16(const void* x, int64_t T, int64_t H, int64_t I, int64_t E, int topk,
+                             const int32_t* topk_ids, const float* topk_w, const uint8_t* w13_codes,
+                             const uint8_t* w13_sf, const float* d_alpha13, const uint8_t* w2_codes,
+                             const uint8_t* w2_sf, const float* d_alpha2, void* out, void* workspace,
+                             size_t ws_bytes, nvfp4_stream_t stream) {
+  nvfp4_status st = moe_w16_check(T, H, I, E, topk);
+  if (st != NVFP4_OK) return st;
+  if (T == 0) return NVFP4_OK;
+  if (!x || !topk_ids || !topk_w || !w13_codes || !w13_sf || !d_alpha13 || !w2_codes || !w2_sf || !d_alpha2 ||
+      !out || !workspace)
+    return NVFP4_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w13_codes) || !aligned16(w13_sf) || !aligned16(w2_codes) || !aligned16(w2_sf) ||
+      !aligned16(out) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(topk_ids) & 3u) ||
+      (reinterpret_cast<uintptr_t>(topk_w) & 3u) || (reinterpret_cast<uintptr_t>(d_alpha13) & 3u) ||
+      (reinterpret_cast<uintptr_t>(d_alpha2) & 3u))
+    return NVFP4_ERR_MISALIGNED;
+  const MoeW16Layout L = moe_w16_layout(T, H, I, E, topk);
+  if (ws_bytes < L.total) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
+  const DeviceInfo* dev = device_info();
+  if (!dev) return NVFP4_ERR_NO_DEVICE;
+  uint8_t* b = static_cast<uint8_t*>(workspace);
+  MoeW16Params p{};
+  p.x = static_cast<const uint16_t*>(x);
+  p.T = static_cast<int>(T);
+  p.H = static_cast<int>(H);
+  p.I = static_cast<int>(I);
+  p.E = static_cast<int>(E);
+  p.topk = topk;
+  p.ids = topk_ids;
+  p.topk_w = topk_w;
+  p.w13_codes = w13_codes;
+  p.w13_sf = w13_sf;
+  p.alpha13 = d_alpha13;
+  p.w2_codes = w2_codes;
+  p.w2_sf = w2_sf;
+  p.alpha2 = d_alpha2;
+  p.out = static_cast<uint16_t*>(out);
+  p.n_slots = reinterpret_cast<int32_t*>(b + L.n_slots);
+  p.slot_expert = reinterpret_cast<int32_t*>(b + L.slot_expert);
+  p.slot_start = reinterpret_cast<int32_t*>(b + L.slot_start);
+  p.slot_count = reinterpret_cast<int32_t*>(b + L.slot_count);
+  p.route_list = reinterpret_cast<int32_t*>(b + L.route_list);
+  p.tok_shift = reinterpret_cast<int32_t*>(b + L.tok_shift);
+  p.h_amax = reinterpret_cast<unsigned int*>(b + L.h_amax);
+  p.h = reinterpret_cast<uint16_t*>(b + L.h);
+  p.partial = reinterpret_cast<float*>(b + L.partial);
+  p.status = dev->status;
+  return cuda_status(launch_moe_w4a16(p, dev->sms, stream));
+}
+
 nvfp4_status nvfp4_moe_calibrate(const void* x_calib, int64_t Tc, int64_t H, int64_t I, int64_t E,
                                  const float* d_g_a1, const uint8_t* w13_codes, const uint8_t* w13_sf,
                                  const float* d_alpha13, float* d_amax, float* d_g_a2, void* workspace,

@@ -44,6 +44,33 @@ cudaError_t launch_moe_dense_ids(int32_t* ids, int64_t Tc, int E, cudaStream_t s
 cudaError_t launch_moe_calib_finish(unsigned int* amax_bits, int E, float* g_max, cudaStream_t stream);
 
 // ---- W4A16 decode (gemv_w4a16.cu) -------------------------------------------
+// W4A16 MoE for small batches (moe_w4a16.cu).  Workspace (device) fields are
+// carved by the API from the caller's workspace.
+struct MoeW16Params {
+  const uint16_t* x;  // [T, H] bf16, contiguous
+  int T, H, I, E, topk;
+  const int32_t* ids;     // [T * topk]
+  const float* topk_w;    // [T * topk]
+  const uint8_t* w13_codes;
+  const uint8_t* w13_sf;
+  const float* alpha13;   // [E]
+  const uint8_t* w2_codes;
+  const uint8_t* w2_sf;
+  const float* alpha2;    // [E]
+  uint16_t* out;          // [T, H] bf16
+  int32_t* n_slots;       // [1]       experts in use
+  int32_t* slot_expert;   // [S]       expert of each slot, ascending
+  int32_t* slot_start;    // [S]       first entry of the slot in route_list
+  int32_t* slot_count;    // [S]       routes of the slot
+  int32_t* route_list;    // [R]       routes grouped by slot, in route order
+  int32_t* tok_shift;     // [T]       power-of-two shift of each token row
+  unsigned int* h_amax;   // [R]       max |h| of each route (fp32 bits)
+  uint16_t* h;            // [R, I]    bf16 intermediate
+  float* partial;         // [R, H]    w * alpha2 * (h @ W2.T) per route
+  int* status;
+};
+cudaError_t launch_moe_w4a16(const MoeW16Params& p, int num_sms, cudaStream_t stream);
+
 struct GemvPlan {
   int splits;      // k-splits (1 = no workspace)
   int kc;          // k elements per split (multiple of 128)
