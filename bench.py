@@ -42,6 +42,7 @@ import synthdata  # noqa: E402
 METRIC = "W4A4 prefill TFLOP/s (frac of FP4 peak); W4A16 decode HBM GB/s at T=1..16"
 PREFILL_M = 8192
 MOE_T = 4096
+MOE16_T = (1, 4, 16)
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio of GB300
 
 
@@ -170,6 +171,19 @@ class Workload:
         self.moe_ws = torch.empty(nv.nvfp4_moe_workspace(MOE_T, H, I, E, topk), dtype=torch.uint8, device=dev)
         self.moe_E, self.moe_I, self.moe_H, self.moe_topk = E, I, H, topk
         self.moe_flops = 2.0 * MOE_T * topk * 3 * H * I
+        # W4A16 MoE for small batches on the same expert banks (decode-sized T)
+        self.moe16_a13 = nv.nvfp4_make_alpha(None, self.moe_W.g13)
+        self.moe16_a2 = nv.nvfp4_make_alpha(None, self.moe_W.g2)
+        ebytes = 2 * I * H // 2 + nv.nvfp4_scale_bytes(2 * I, H) + H * I // 2 + nv.nvfp4_scale_bytes(H, I)
+        self.moe16 = []
+        for T in MOE16_T:
+            c = synthdata.moe_case(T, E, H, I, topk, cfg["skewed"], seed=T, device=dev)
+            used = int(torch.unique(c.topk_ids).numel())
+            self.moe16.append(dict(T=T, x=c.x, ids=c.topk_ids, w=c.topk_w, experts=used,
+                                   out=torch.empty(T, H, dtype=torch.bfloat16, device=dev),
+                                   ws=torch.empty(nv.nvfp4_moe_w4a16_workspace(T, H, I, E, topk), dtype=torch.uint8,
+                                                  device=dev),
+                                   bytes=used * ebytes + 2 * T * H * 2))
         self.flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
 
@@ -192,6 +206,11 @@ class Workload:
                                self.moe_W.w13_sf, self.moe_a13, self.moe_g_a2, self.moe_W.w2_codes,
                                self.moe_W.w2_sf, self.moe_a2, self.moe_E, self.moe_I, out=self.moe_out,
                                workspace=self.moe_ws)
+
+    def moe16_call(self, c):
+        self.nv.nvfp4_moe_w4a16(c["x"], c["ids"], c["w"], self.moe_W.w13_codes, self.moe_W.w13_sf, self.moe16_a13,
+                                self.moe_W.w2_codes, self.moe_W.w2_sf, self.moe16_a2, self.moe_E, self.moe_I,
+                                out=c["out"], workspace=c["ws"])
 
     def build_decode_graphs(self):
         lib = self.lib
@@ -222,7 +241,7 @@ class Workload:
         self.flush_buf.fill_(1)
 
     def launches_per_step(self) -> int:
-        return 3 + sum(d["ncopy"] * d["launches"] for d in self.decode) + 7
+        return 3 + sum(d["ncopy"] * d["launches"] for d in self.decode) + 7 + 3 * len(self.moe16)
 
 
 def _profile_traffic(name: str):
@@ -276,8 +295,12 @@ def run_ours(args, world, rank, local):
             dec.append(_timed(d["graph"].replay, stream))
         wl.flush()
         ev_moe = _timed(wl.moe, stream)
+        m16 = []
+        for c in wl.moe16:
+            wl.flush()
+            m16.append(_timed(lambda c=c: wl.moe16_call(c), stream))
         if record is not None:
-            record.append((ev_pre, ev_gemm, dec, ev_moe, ev_quant))
+            record.append((ev_pre, ev_gemm, dec, ev_moe, ev_quant, m16))
 
     for _ in range(args.warmup):
         step(None)
@@ -300,7 +323,8 @@ def run_ours(args, world, rank, local):
     gemm_ms = [ms(r[1]) for r in recs]
     moe_ms = [ms(r[3]) for r in recs]
     dec_ms = [[ms(e) for e in r[2]] for r in recs]
-    step_ms = [p + g + sum(d) + m for p, g, d, m in zip(pre_ms, gemm_ms, dec_ms, moe_ms)]
+    m16_ms = [[ms(e) for e in r[5]] for r in recs]
+    step_ms = [p + g + sum(d) + m + sum(q) for p, g, d, m, q in zip(pre_ms, gemm_ms, dec_ms, moe_ms, m16_ms)]
     t_pre = statistics.median(pre_ms) * 1e-3
     t_gemm = statistics.median(gemm_ms) * 1e-3
     t_moe = statistics.median(moe_ms) * 1e-3
@@ -318,6 +342,11 @@ def run_ours(args, world, rank, local):
         decode[f"T{d['T']}_{d['N']}x{d['K']}"] = {
             "us": round(t * 1e6, 3), "gbs": round(d["bytes"] / t / 1e9, 1),
             "frac_hbm": round(d["bytes"] / t / 1e9 / hbm, 4)}
+    moe16 = {}
+    for i, c in enumerate(wl.moe16):
+        t = statistics.median([x[i] for x in m16_ms]) * 1e-3
+        moe16[f"T{c['T']}"] = {"us": round(t * 1e6, 2), "experts": c["experts"], "gbs": round(c["bytes"] / t / 1e9, 1),
+                               "frac_hbm": round(c["bytes"] / t / 1e9 / hbm, 4)}
     head_key = f"T1_{synthdata.DECODE_SHAPES[0][0]}x{synthdata.DECODE_SHAPES[0][1]}"
     head = decode[head_key]
     head_bytes = next(d["bytes"] for d in wl.decode if d["T"] == 1 and (d["N"], d["K"]) == synthdata.DECODE_SHAPES[0])
@@ -331,6 +360,7 @@ def run_ours(args, world, rank, local):
         "config": {"workload": "fused qkv W4A4 prefill M=8192 N=5120+1024+1024 K=5120 (quant + GEMM)",
                    "decode": "W4A16 T=1..16 on 8704x5120 and 5120x4352, cold weights in CUDA graphs",
                    "moe": "W4A4 MoE E=128 top8 H=2048 I=768 T=4096",
+                   "moe_w4a16": "W4A16 MoE E=128 top8 H=2048 I=768 T=1, 4, 16 (bytes: the touched experts' weights)",
                    "l2": "flushed (256 MiB write) before every stage, outside the timed events",
                    "parallelism": f"replicas x{world}"},
         "prefill": {"ms": round(t_pre * 1e3, 4), "tflops": round(wl.pre_flops / t_pre / 1e12, 1),
@@ -342,6 +372,7 @@ def run_ours(args, world, rank, local):
         "decode": decode,
         "moe": {"ms": round(t_moe * 1e3, 4), "tflops": round(wl.moe_flops / t_moe / 1e12, 1),
                 "frac_fp4_peak": round(wl.moe_flops / t_moe / 1e12 / fp4_peak, 4)},
+        "moe_w4a16": moe16,
         # the dominant kernel of the step (about 95 % of its device time, see
         # profiles/launches_bench_step.md) is the decode GEMM; its roofline is
         # given for the headline decode call, T = 1 on 8704 x 5120
@@ -553,6 +584,18 @@ def run_profile(stage: str, reps: int):
         for _ in range(reps):
             nv.nvfp4_moe_w4a4(mc.x, mc.topk_ids, mc.topk_w, g1, Wm.w13_codes, Wm.w13_sf, a13, g2, Wm.w2_codes,
                               Wm.w2_sf, a2, E, I, out=out, workspace=ws)
+    elif stage == "moe16":
+        cfg = synthdata.MOE_SMALL
+        E, H, I, topk = cfg["E"], cfg["H"], cfg["I"], cfg["topk"]
+        mc = synthdata.moe_case(4, E, H, I, topk, cfg["skewed"], seed=4, device=dev)
+        Wm = nv.quantize_moe_weights(lambda e: mc.w13(e), lambda e: mc.w2(e), E, H, I, dev)
+        a13 = nv.nvfp4_make_alpha(None, Wm.g13)
+        a2 = nv.nvfp4_make_alpha(None, Wm.g2)
+        out = torch.empty(4, H, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(nv.nvfp4_moe_w4a16_workspace(4, H, I, E, topk), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            nv.nvfp4_moe_w4a16(mc.x, mc.topk_ids, mc.topk_w, Wm.w13_codes, Wm.w13_sf, a13, Wm.w2_codes, Wm.w2_sf,
+                               a2, E, I, out=out, workspace=ws)
     else:
         raise SystemExit(f"unknown stage {stage}")
     torch.cuda.synchronize()
@@ -567,7 +610,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["gemm", "quant", "gemv", "moe"],
+    ap.add_argument("--profile", choices=["gemm", "quant", "gemv", "moe", "moe16"],
                     help="launch one stage a few times on a small case (for ncu), print nothing else")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()

@@ -233,15 +233,19 @@ nvfp4_status nvfp4_moe_calibrate(const void* x_calib_bf16, int64_t Tc, int64_t H
  * and weights as nvfp4_moe_w4a4; ids outside [0, E) set
  * NVFP4_ERR_BAD_EXPERT_ID in the device word and are dropped.
  * Shapes: 1 <= T <= 64, 1 <= topk <= 8, H % 128 == 0, I % 128 == 0,
- * E <= 1024; T = 0 returns NVFP4_OK with no launch.  The result is
- * deterministic (no atomics in the sums).
+ * H <= 16384, I <= 16384, E <= 1024; T = 0 returns NVFP4_OK with no launch.
+ * w13_codes, w13_sf, w2_codes, w2_sf, out and workspace 16-byte aligned;
+ * ids, weights and alphas 4-byte aligned (else NVFP4_ERR_MISALIGNED).  The
+ * result is deterministic (no atomics in the sums).
  * --------------------------------------------------------------------------- */
 
-/* Workspace bytes of nvfp4_moe_w4a16 for T tokens. */
+/* Workspace bytes of nvfp4_moe_w4a16 for T tokens (fp32 gate_up sums and
+ * down partials of every route); 0 for an unsupported shape. */
 size_t nvfp4_moe_w4a16_workspace(int64_t T, int64_t H, int64_t I, int64_t E, int topk);
 
-/* route -> gate_up (SiLU * up, bf16 h) -> down (routing weight) -> slot sum
- * -> bf16.  No host synchronisation. */
+/* gate_up (fp32 G, U per route) -> down (h staged from G, U; routing
+ * weight) -> slot sum -> bf16: three kernels chained by programmatic
+ * dependent launch.  No host synchronisation. */
 nvfp4_status nvfp4_moe_w4a16(const void* x_bf16, int64_t T, int64_t H, int64_t I, int64_t E, int topk,
                              const int32_t* topk_ids, const float* topk_w, const uint8_t* w13_codes,
                              const uint8_t* w13_sf, const float* d_alpha13, const uint8_t* w2_codes,

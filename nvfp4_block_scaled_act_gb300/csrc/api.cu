@@ -423,26 +423,19 @@ nvfp4_status nvfp4_moe_w4a4(const void* x, int64_t T, int64_t H, int64_t I, int6
 
 namespace {
 struct MoeW16Layout {
-  size_t n_slots, slot_expert, slot_start, slot_count, route_list, tok_shift, h_amax, h, partial, total;
+  size_t gu, partial, total;
 };
 MoeW16Layout moe_w16_layout(int64_t T, int64_t H, int64_t I, int64_t E, int topk) {
   MoeW16Layout L{};
+  (void)E;
   const int64_t R = T * topk;
-  const int64_t S = R < E ? R : E;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
     off = align256(off + bytes);
     return o;
   };
-  L.n_slots = take(sizeof(int32_t));
-  L.slot_expert = take(static_cast<size_t>(S) * sizeof(int32_t));
-  L.slot_start = take(static_cast<size_t>(S) * sizeof(int32_t));
-  L.slot_count = take(static_cast<size_t>(S) * sizeof(int32_t));
-  L.route_list = take(static_cast<size_t>(R) * sizeof(int32_t));
-  L.tok_shift = take(static_cast<size_t>(T) * sizeof(int32_t));
-  L.h_amax = take(static_cast<size_t>(R) * sizeof(uint32_t));
-  L.h = take(static_cast<size_t>(R * I) * sizeof(uint16_t));
+  L.gu = take(static_cast<size_t>(R * 2 * I) * sizeof(float));
   L.partial = take(static_cast<size_t>(R * H) * sizeof(float));
   L.total = off;
   return L;
@@ -450,7 +443,7 @@ MoeW16Layout moe_w16_layout(int64_t T, int64_t H, int64_t I, int64_t E, int topk
 nvfp4_status moe_w16_check(int64_t T, int64_t H, int64_t I, int64_t E, int topk) {
   if (T < 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0) return NVFP4_ERR_INVALID_ARG;
   if (T > 64 || topk > 8 || H % 128 != 0 || I % 128 != 0 || E > 1024) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  if (H > (1 << 16) || I > (1 << 16) || E * 2 * I > (1LL << 30) || E * H > (1LL << 30))
+  if (H > (1 << 14) || I > (1 << 14) || E * 2 * I > (1LL << 30) || E * H > (1LL << 30))
     return NVFP4_ERR_UNSUPPORTED_SHAPE;
   return NVFP4_OK;
 }
@@ -491,24 +484,18 @@ nvfp4_status nvfp4_moe_w4a16(const void* x, int64_t T, int64_t H, int64_t I, int
   p.topk = topk;
   p.ids = topk_ids;
   p.topk_w = topk_w;
-  p.w13_codes = w13_codes;
   p.w13_sf = w13_sf;
   p.alpha13 = d_alpha13;
-  p.w2_codes = w2_codes;
   p.w2_sf = w2_sf;
   p.alpha2 = d_alpha2;
   p.out = static_cast<uint16_t*>(out);
-  p.n_slots = reinterpret_cast<int32_t*>(b + L.n_slots);
-  p.slot_expert = reinterpret_cast<int32_t*>(b + L.slot_expert);
-  p.slot_start = reinterpret_cast<int32_t*>(b + L.slot_start);
-  p.slot_count = reinterpret_cast<int32_t*>(b + L.slot_count);
-  p.route_list = reinterpret_cast<int32_t*>(b + L.route_list);
-  p.tok_shift = reinterpret_cast<int32_t*>(b + L.tok_shift);
-  p.h_amax = reinterpret_cast<unsigned int*>(b + L.h_amax);
-  p.h = reinterpret_cast<uint16_t*>(b + L.h);
+  p.gu = reinterpret_cast<float*>(b + L.gu);
   p.partial = reinterpret_cast<float*>(b + L.partial);
   p.status = dev->status;
-  return cuda_status(launch_moe_w4a16(p, dev->sms, stream));
+  CUtensorMap m13, m2;
+  if (!make_gemv_codes_map(&m13, w13_codes, E * 2 * I, H / 2) || !make_gemv_codes_map(&m2, w2_codes, E * H, I / 2))
+    return NVFP4_ERR_CUDA;
+  return cuda_status(launch_moe_w4a16(m13, m2, p, dev->sms, stream));
 }
 
 nvfp4_status nvfp4_moe_calibrate(const void* x_calib, int64_t Tc, int64_t H, int64_t I, int64_t E,

@@ -276,28 +276,6 @@ constexpr int kRingSlot = kRingChunk + kRingChunkSf;
 constexpr int kRingMaxCluster = 8;
 constexpr size_t kRingSmemBudget = 109 * 1024;        // two CTAs per SM with their static shared memory
 
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 template <bool kTok16>
 __global__ void __launch_bounds__(RingShape<kTok16>::kThreads, RingShape<kTok16>::kMinBlocks) gemv_ring_kernel(
     const __grid_constant__ CUtensorMap cmap, const uint16_t* __restrict__ x, int T, int64_t ldx,

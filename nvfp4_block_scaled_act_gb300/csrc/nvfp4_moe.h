@@ -51,25 +51,30 @@ struct MoeW16Params {
   int T, H, I, E, topk;
   const int32_t* ids;     // [T * topk]
   const float* topk_w;    // [T * topk]
-  const uint8_t* w13_codes;
-  const uint8_t* w13_sf;
+  const uint8_t* w13_sf;  // codes are read through the tensor maps
   const float* alpha13;   // [E]
-  const uint8_t* w2_codes;
   const uint8_t* w2_sf;
   const float* alpha2;    // [E]
   uint16_t* out;          // [T, H] bf16
-  int32_t* n_slots;       // [1]       experts in use
-  int32_t* slot_expert;   // [S]       expert of each slot, ascending
-  int32_t* slot_start;    // [S]       first entry of the slot in route_list
-  int32_t* slot_count;    // [S]       routes of the slot
-  int32_t* route_list;    // [R]       routes grouped by slot, in route order
-  int32_t* tok_shift;     // [T]       power-of-two shift of each token row
-  unsigned int* h_amax;   // [R]       max |h| of each route (fp32 bits)
-  uint16_t* h;            // [R, I]    bf16 intermediate
+  float* gu;              // [R, 2I]   gate_up sums of each route (fp32, alpha not applied)
   float* partial;         // [R, H]    w * alpha2 * (h @ W2.T) per route
   int* status;
 };
-cudaError_t launch_moe_w4a16(const MoeW16Params& p, int num_sms, cudaStream_t stream);
+
+// Launch shape of one grouped GEMV stage: CTA (slot, 128-row block, k-split)
+// in clusters of `cl` k-splits over `kc` k elements each, a ring of R 128-k
+// weight blocks per CTA, and passes of 8 or 16 routes (tok16).
+struct Moe16Plan {
+  int cl, kc, R, nrb;
+  bool tok16;
+  size_t smem;  // dynamic shared memory per CTA
+  bool ok;
+};
+Moe16Plan moe16_plan(int64_t K, int64_t rows_per_expert, int64_t slots, int64_t T, int num_sms);
+// w13_map / w2_map: the stacked code matrices [E*2I, H/2] and [E*H, I/2] as
+// boxes of 64 bytes x 128 rows (make_gemv_codes_map).
+cudaError_t launch_moe_w4a16(const CUtensorMap& w13_map, const CUtensorMap& w2_map, const MoeW16Params& p,
+                             int num_sms, cudaStream_t stream);
 
 struct GemvPlan {
   int splits;      // k-splits (1 = no workspace)
