@@ -80,14 +80,14 @@ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 }  // namespace
 
-// Codes of the decode weight: boxes of 64 bytes (one 128-k block) x 128 rows,
-// no swizzle; rows past N read as zero codes.
-bool make_gemv_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes) {
+// Codes of a W4A16 weight: boxes of 64 bytes (one 128-k block) x box_rows
+// rows, no swizzle; rows past the end read as zero codes.
+bool make_gemv_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -423,7 +423,7 @@ nvfp4_status nvfp4_moe_w4a4(const void* x, int64_t T, int64_t H, int64_t I, int6
 
 namespace {
 struct MoeW16Layout {
-  size_t gu, partial, total;
+  size_t h, dn, total;
 };
 MoeW16Layout moe_w16_layout(int64_t T, int64_t H, int64_t I, int64_t E, int topk) {
   MoeW16Layout L{};
@@ -435,8 +435,8 @@ MoeW16Layout moe_w16_layout(int64_t T, int64_t H, int64_t I, int64_t E, int topk
     off = align256(off + bytes);
     return o;
   };
-  L.gu = take(static_cast<size_t>(R * 2 * I) * sizeof(float));
-  L.partial = take(static_cast<size_t>(R * H) * sizeof(float));
+  L.h = take(static_cast<size_t>(R * I) * sizeof(uint16_t));
+  L.dn = take(static_cast<size_t>(R * H) * sizeof(float));
   L.total = off;
   return L;
 }
@@ -444,6 +444,8 @@ nvfp4_status moe_w16_check(int64_t T, int64_t H, int64_t I, int64_t E, int topk)
   if (T < 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0) return NVFP4_ERR_INVALID_ARG;
   if (T > 64 || topk > 8 || H % 128 != 0 || I % 128 != 0 || E > 1024) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (H > (1 << 14) || I > (1 << 14) || E * 2 * I > (1LL << 30) || E * H > (1LL << 30))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && (!moe16_plan(0, H, T, E, topk, I / 64, 1).ok || !moe16_plan(1, I, T, E, topk, H / 128, 1).ok))
     return NVFP4_ERR_UNSUPPORTED_SHAPE;
   return NVFP4_OK;
 }
@@ -489,11 +491,11 @@ nvfp4_status nvfp4_moe_w4a16(const void* x, int64_t T, int64_t H, int64_t I, int
   p.w2_sf = w2_sf;
   p.alpha2 = d_alpha2;
   p.out = static_cast<uint16_t*>(out);
-  p.gu = reinterpret_cast<float*>(b + L.gu);
-  p.partial = reinterpret_cast<float*>(b + L.partial);
+  p.h = reinterpret_cast<uint16_t*>(b + L.h);
+  p.dn = reinterpret_cast<float*>(b + L.dn);
   p.status = dev->status;
   CUtensorMap m13, m2;
-  if (!make_gemv_codes_map(&m13, w13_codes, E * 2 * I, H / 2) || !make_gemv_codes_map(&m2, w2_codes, E * H, I / 2))
+  if (!make_gemv_codes_map(&m13, w13_codes, E * 2 * I, H / 2, 64) || !make_gemv_codes_map(&m2, w2_codes, E * H, I / 2))
     return NVFP4_ERR_CUDA;
   return cuda_status(launch_moe_w4a16(m13, m2, p, dev->sms, stream));
 }

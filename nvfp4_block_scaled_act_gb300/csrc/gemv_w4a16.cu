@@ -472,6 +472,7 @@ __global__ void __launch_bounds__(RingShape<kTok16>::kThreads, RingShape<kTok16>
         cw[j] = *reinterpret_cast<const uint4*>(cs + cofs[j]);
         scale_pair_f16(*reinterpret_cast<const uint16_t*>(ss + sf_off[j]), slo[j], shi[j]);
       }
+      fence_proxy_async_smem_read();
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       s += kGroups;
@@ -578,6 +579,11 @@ GemvRingPlan gemv_ring_plan(int64_t T, int64_t N, int64_t K, int num_sms) {
   int64_t slots = fixed < kRingSmemBudget ? static_cast<int64_t>((kRingSmemBudget - fixed) / kRingSlot) : 0;
   if (slots > kcb) slots = kcb;
   if (slots > kRingMaxSlots) slots = kRingMaxSlots;
+  // a ring that is refilled is even: each slot then stays with one k-group
+  // (kb and kb + R have the same parity), so no warp waits on a slot two
+  // phases ahead of the last one it read, where the mbarrier parity test
+  // would pass on a stale phase
+  if (slots < kcb && slots > 1) slots &= ~int64_t{1};
   p.R = static_cast<int>(slots);
   p.ok = slots >= 2 || (slots >= 1 && kcb == 1);
   p.smem = fixed + static_cast<size_t>(slots) * kRingSlot + 1024;  // + alignment slack

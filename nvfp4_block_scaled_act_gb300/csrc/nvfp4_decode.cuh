@@ -63,6 +63,13 @@ __device__ __forceinline__ int token_shift(unsigned int amax_bits) {
 }
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
 
+// A consumer that read a ring slot with ordinary shared-memory loads releases
+// it to a TMA refill (async proxy) only after this fence: without it the
+// refill was seen to overwrite data that the loads had not yet returned.
+__device__ __forceinline__ void fence_proxy_async_smem_read() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Programmatic dependent launch, thread-block clusters and named barriers.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -56,23 +56,24 @@ struct MoeW16Params {
   const uint8_t* w2_sf;
   const float* alpha2;    // [E]
   uint16_t* out;          // [T, H] bf16
-  float* gu;              // [R, 2I]   gate_up sums of each route (fp32, alpha not applied)
-  float* partial;         // [R, H]    w * alpha2 * (h @ W2.T) per route
+  uint16_t* h;            // [R, I]  bf16 silu(a13 G) * (a13 U) of every route
+  float* dn;              // [R, H]  w * a2 * (h @ W2[e].T) of every route
   int* status;
 };
 
-// Launch shape of one grouped GEMV stage: CTA (slot, 128-row block, k-split)
-// in clusters of `cl` k-splits over `kc` k elements each, a ring of R 128-k
-// weight blocks per CTA, and passes of 8 or 16 routes (tok16).
+// Launch shape of one grouped GEMV stage.  Work items are (slot, row block);
+// `ctas` persistent CTAs take items round-robin and stream their weights
+// through a ring of R 128-k blocks; activations are staged in windows of
+// `win` k elements, 16 route rows at a time if tok16, else 8.
 struct Moe16Plan {
-  int cl, kc, R, nrb;
+  int win, R, ctas;
   bool tok16;
   size_t smem;  // dynamic shared memory per CTA
   bool ok;
 };
-Moe16Plan moe16_plan(int64_t K, int64_t rows_per_expert, int64_t slots, int64_t T, int num_sms);
-// w13_map / w2_map: the stacked code matrices [E*2I, H/2] and [E*H, I/2] as
-// boxes of 64 bytes x 128 rows (make_gemv_codes_map).
+Moe16Plan moe16_plan(int mode, int64_t K, int64_t T, int64_t E, int topk, int64_t units, int num_sms);
+// w13_map: the stacked gate/up codes [E*2I, H/2] as boxes of 64 bytes x 64
+// rows; w2_map: the down codes [E*H, I/2] as boxes of 64 bytes x 128 rows.
 cudaError_t launch_moe_w4a16(const CUtensorMap& w13_map, const CUtensorMap& w2_map, const MoeW16Params& p,
                              int num_sms, cudaStream_t stream);
 

@@ -134,6 +134,17 @@ def test_moe_w4a16_one_expert_for_all_routes(nv, small):
     check_close(out.cpu(), small.ref(c.x, ids, c.topk_w), "W4A16 MoE one expert")
 
 
+@pytest.mark.parametrize("T", [4, 16, 64])
+def test_moe_w4a16_bitwise_repeatable(nv, small, T):
+    """The same call gives the same bits every time: every sum has a fixed
+    order, and a weight-ring slot is refilled only after the reads of the
+    previous block are complete (the large-workload case below too)."""
+    c = synthdata.moe_case(T, S["E"], S["H"], S["I"], S["topk"], S["skewed"], seed=40 + T, device=DEV)
+    runs = [small.gpu(nv, c.x, c.topk_ids, c.topk_w) for _ in range(6)]
+    for r in runs[1:]:
+        assert torch.equal(r, runs[0]), f"W4A16 MoE T={T} is not repeatable"
+
+
 def test_moe_w4a16_top1_and_repeatable(nv, small):
     c = synthdata.moe_case(5, S["E"], S["H"], S["I"], 1, S["skewed"], seed=13, device="cpu")
     a = small.gpu(nv, c.x, c.topk_ids, c.topk_w)
@@ -165,3 +176,13 @@ def test_moe_w4a16_large_workload(nv, large, T):
     out = bank.gpu(nv, c.x, c.topk_ids, c.topk_w)
     assert nv.nvfp4_device_status() == 0
     check_close(out.cpu(), bank.ref(c.x, c.topk_ids, c.topk_w), f"W4A16 MoE large T={T}")
+    for _ in range(5):
+        assert torch.equal(bank.gpu(nv, c.x, c.topk_ids, c.topk_w), out), f"W4A16 MoE large T={T} is not repeatable"
+
+
+def test_moe_w4a16_large_workload_repeatable(nv, large):
+    c = synthdata.moe_case(16, L["E"], L["H"], L["I"], L["topk"], L["skewed"], seed=16, device="cpu")
+    runs = [large.gpu(nv, c.x, c.topk_ids, c.topk_w) for _ in range(6)]
+    assert nv.nvfp4_device_status() == 0
+    for r in runs[1:]:
+        assert torch.equal(r, runs[0]), "W4A16 MoE large T=16 is not repeatable"
