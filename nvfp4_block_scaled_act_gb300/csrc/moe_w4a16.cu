@@ -31,7 +31,7 @@ namespace nvfp4 {
 constexpr int kM16Groups = 2;                       // k-groups (128-k blocks dealt by parity)
 constexpr int kM16CompWarps = 4 * kM16Groups;       // 4 row groups of 32 x 2 k-groups
 constexpr int kM16Comp = kM16CompWarps * 32;
-constexpr int kM16Threads = kM16Comp + 32;          // + one producer warp
+constexpr int kM16Threads = kM16Comp + 64;          // + a code and a scale producer warp
 constexpr int kM16Rows = 128;                       // weight rows per item
 constexpr int kM16Chunk = kM16Rows * 64;            // codes of one 128-k block
 constexpr int kM16MaxSlots = 24;
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kM16Threads, 2)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < Rs; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full[i], 2);  // the code and the scale producer
       mbar_init(&empty[i], 4);
     }
     fence_barrier_init();
@@ -149,9 +149,13 @@ __global__ void __launch_bounds__(kM16Threads, 2)
     return MODE == 0 ? e * 2 * p.I + 64 * unit : e * p.H + kM16Rows * unit;
   };
 
-  if (warp == kM16CompWarps) {
-    // --- producer warp: lane 0 streams the weights, the warp counts routes ----
-    if (lane == 0) prefetch_tmap(&cmap);
+  if (warp >= kM16CompWarps) {
+    // --- producer warps: lane 0 of the first streams the codes, of the second
+    // the scales (every copy costs its issuing lane a few hundred cycles, so
+    // two lanes keep the ring full at twice the rate); the warps count the
+    // routes of every item
+    const bool codes = warp == kM16CompWarps;
+    if (codes && lane == 0) prefetch_tmap(&cmap);
     const uint8_t* wsf = MODE == 0 ? p.w13_sf : p.w2_sf;
     int q = 0;
     bool ok = true;
@@ -170,15 +174,14 @@ __global__ void __launch_bounds__(kM16Threads, 2)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full[s], kSlot);
-            if (MODE == 0) {
+            if (codes) {
+              mbar_arrive_expect_tx(&full[s], kM16Chunk);
               tma_load_2d(ring + s * kM16Chunk, &cmap, &full[s], kb * 64, g0);
-              tma_load_2d(ring + s * kM16Chunk + kM16Chunk / 2, &cmap, &full[s], kb * 64, g0 + p.I);
-              bulk_load(ring_sf + s * kSf, sf0 + kb * 1024, 1024, &full[s]);
-              bulk_load(ring_sf + s * kSf + 1024, sf1 + kb * 1024, 1024, &full[s]);
+              if (MODE == 0) tma_load_2d(ring + s * kM16Chunk + kM16Chunk / 2, &cmap, &full[s], kb * 64, g0 + p.I);
             } else {
-              tma_load_2d(ring + s * kM16Chunk, &cmap, &full[s], kb * 64, g0);
+              mbar_arrive_expect_tx(&full[s], kSf);
               bulk_load(ring_sf + s * kSf, sf0 + kb * 1024, 1024, &full[s]);
+              if (MODE == 0) bulk_load(ring_sf + s * kSf + 1024, sf1 + kb * 1024, 1024, &full[s]);
             }
           }
         }
