@@ -397,7 +397,7 @@ def run_ours(args, world, rank, local):
         "moe": {"ms": round(t_moe * 1e3, 4), "tflops": round(wl.moe_flops / t_moe / 1e12, 1),
                 "frac_fp4_peak": round(wl.moe_flops / t_moe / 1e12 / fp4_peak, 4)},
         "moe_w4a16": moe16,
-        # the dominant kernel of the step (about 95 % of its device time, see
+        # the dominant kernel of the step (about 90 % of its device time, see
         # profiles/launches_bench_step.md) is the decode GEMM; its roofline is
         # given for the headline decode call, T = 1 on 8704 x 5120
         "roofline": {"kernel": "gemv_ring_kernel<0> (W4A16 decode, T=1, 8704x5120)", "bound": "hbm",
