@@ -97,6 +97,37 @@ def test_moe_workspace_layout(lib):
     assert f(*args) == 2   # H % 128
 
 
+def test_moe_w4a16_argument_errors(lib):
+    ws = lib.nvfp4_moe_w4a16_workspace
+    R = 4 * 8
+    assert ws(4, 2048, 768, 128, 8) == R * 768 * 2 + R * 2048 * 4   # bf16 h, fp32 per-route down rows
+    assert ws(65, 2048, 768, 128, 8) == 0      # T > 64: the W4A4 path's regime
+    assert ws(4, 2048, 768, 128, 9) == 0       # topk > 8
+    assert ws(4, 2000, 768, 128, 8) == 0       # H % 128
+    assert ws(4, 2048, 768, 1025, 8) == 0      # E > 1024
+    f = lib.nvfp4_moe_w4a16
+    big = ctypes.c_size_t(1 << 40)
+    args = [P, 4, 2048, 768, 128, 8] + [P] * 10 + [big, None]
+    args[2] = 2000
+    assert f(*args) == 2                       # H % 128
+    args[2] = 2048
+    args[1] = 0
+    assert f(*args) == 0                       # T = 0: nothing to do
+    args[1] = 4
+    args[6] = None
+    assert f(*args) == 1                       # null ids
+    args[6] = P
+    args[8] = ctypes.c_void_p(260)
+    assert f(*args) == 3                       # misaligned W13 codes
+    args[8] = P
+    args[-2] = ctypes.c_size_t(16)
+    assert f(*args) == 4                       # workspace too small
+    import torch
+    if not torch.cuda.is_available():
+        args[-2] = big
+        assert f(*args) == 8                   # valid arguments, no device
+
+
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         nv.load_library.__wrapped__ if hasattr(nv.load_library, "__wrapped__") else None
