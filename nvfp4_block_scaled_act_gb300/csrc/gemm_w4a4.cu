@@ -675,6 +675,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     regs_dec();
     if (warp == 0 || warp == 2) {
       // ---------------------------------------------------------- producers
+      // The kernel starts under programmatic dependent launch: everything above
+      // (barriers, TMEM, descriptors) overlaps the preceding kernel's tail; the
+      // activations and their scales are read only after it has finished.
+      pdl_wait();
       const bool scale_role = warp == 2;
       uint32_t it = 0;
       bool ok = true;
@@ -865,6 +869,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int part = ew >> 2;    // column half: 128 part ..
     uint8_t* stg = smem + STAGES * Cfg::STAGE_BYTES + ew * Cfg::EPI_WARP_BYTES;
     const uint32_t acce_lead = mapa_shared(&acce_bar, 0);
+    pdl_wait();  // alpha (and the output buffer) may belong to the preceding kernel
     const float alpha = __ldg(p.alpha);
     uint32_t acc_phase = 0;
     for (int tile = unit0; tile < total; tile += unit_step) {
@@ -951,8 +956,17 @@ cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int
         attr_set = true;
       }
       if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;  // whole CTA pairs
-      gemm_pair_kernel<<<grid, kThreads, PairCfg::SMEM_BYTES, stream>>>(maps.a, maps.b, maps.out, p);
-      return cudaGetLastError();
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(grid));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, gemm_pair_kernel, maps.a, maps.b, maps.out, p);
     }
     case kEpiGatedQuant: return launch_cfg<GatedCfg>(maps, p, grid, stream);
     case kEpiGatedAmax: return launch_cfg<AmaxCfg>(maps, p, grid, stream);

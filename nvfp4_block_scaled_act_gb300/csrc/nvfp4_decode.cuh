@@ -70,9 +70,7 @@ __device__ __forceinline__ void fence_proxy_async_smem_read() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Programmatic dependent launch, thread-block clusters and named barriers.
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Thread-block clusters and named barriers.
 
 __device__ __forceinline__ uint32_t cluster_nctarank() {
   uint32_t r;

@@ -60,6 +60,9 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restri
                                                         uint8_t* __restrict__ codes,
                                                         uint8_t* __restrict__ scales, int64_t Mp, int64_t C,
                                                         int64_t Cp) {
+  // a GEMM launched after this kernel with programmatic dependent launch may
+  // set up while this one runs; it reads the codes only after this grid ends
+  pdl_launch_dependents();
   // r = g / S for every E4M3 scale byte S (IEEE division, as in the block rule)
   __shared__ float r_of_s8[256];
   const float g = __ldg(d_global);
