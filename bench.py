@@ -282,6 +282,22 @@ def _profile_traffic(name: str):
         return None
 
 
+def max_over_ranks(values, world: int, device="cpu"):
+    """The slowest replica bounds the job: element-wise max of per-rank times
+    over all ranks (any backend: NCCL on GPUs, gloo on CPU)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_throughput(world: int, units_per_rank: float, seconds: float) -> float:
+    """Weak scaling: every rank processes the same units; the job's rate is all
+    ranks' units over the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 def _timed(fn, stream):
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
@@ -353,10 +369,7 @@ def run_ours(args, world, rank, local):
     t_moe = statistics.median(moe_ms) * 1e-3
     t_quant = statistics.median([ms(r[4]) for r in recs]) * 1e-3
     per_step = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([t_pre, per_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_pre, per_step = float(t[0]), float(t[1])
+    t_pre, per_step = max_over_ranks([t_pre, per_step], world, dev)
     hbm, bf16, bf16_sus, peak_src = _peaks()
     fp4_peak = bf16 * FP4_OVER_BF16
     decode = {}
@@ -373,7 +386,7 @@ def run_ours(args, world, rank, local):
     head_key = f"T1_{synthdata.DECODE_SHAPES[0][0]}x{synthdata.DECODE_SHAPES[0][1]}"
     head = decode[head_key]
     head_bytes = next(d["bytes"] for d in wl.decode if d["T"] == 1 and (d["N"], d["K"]) == synthdata.DECODE_SHAPES[0])
-    value = world * wl.pre_flops / t_pre / 1e12
+    value = job_throughput(world, wl.pre_flops, t_pre) / 1e12
     gemm_tflops = wl.pre_flops / t_gemm / 1e12
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
