@@ -275,6 +275,13 @@ typedef struct {
 nvfp4_status nvfp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int topk,
                                         nvfp4_moe_layout* host_layout);
 
+/* Self-test of the device timeout path: launches one CTA whose pipeline wait
+ * (the bounded mbarrier wait every kernel uses) has nobody to complete it.
+ * The wait gives up after about a second and records NVFP4_ERR_DEVICE_TIMEOUT
+ * in the device status word; the CTA then exits normally and the context
+ * stays usable.  No fault, trap or unbounded wait is involved. */
+nvfp4_status nvfp4_selftest_wait_timeout(nvfp4_stream_t stream);
+
 /* Synchronises `stream`, copies the device status word to *host_out (an
  * nvfp4_status value, NVFP4_OK if nothing was flagged) and clears it. */
 nvfp4_status nvfp4_device_status(nvfp4_stream_t stream, int32_t* host_out);

@@ -69,6 +69,7 @@ SIGNATURES = {
     "nvfp4_moe_w4a16": (_ST, [_P, _I64, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                               _P]),
     "nvfp4_device_status": (_ST, [_P, ctypes.POINTER(ctypes.c_int32)]),
+    "nvfp4_selftest_wait_timeout": (_ST, [_P]),
 }
 
 _lock = threading.Lock()
@@ -264,6 +265,12 @@ def nvfp4_moe_calibrate(x_calib, g_a1, w13_codes, w13_sf, alpha13, E: int, I: in
         _ptr(x_calib), Tc, H, I, E, _ptr(g_a1), _ptr(w13_codes), _ptr(w13_sf), _ptr(alpha13),
         _ptr(amax), _ptr(g_a2), _ptr(workspace), workspace.numel(), _stream(stream)))
     return g_a2, amax
+
+
+def nvfp4_selftest_wait_timeout(stream=None) -> None:
+    """Launch the timeout self-test: one CTA's bounded pipeline wait runs out
+    (about a second) and the device status word reads NVFP4_ERR_DEVICE_TIMEOUT."""
+    _check("nvfp4_selftest_wait_timeout", load_library().nvfp4_selftest_wait_timeout(_stream(stream)))
 
 
 def nvfp4_device_status(stream=None) -> int:

@@ -194,6 +194,21 @@ static nvfp4_status launch_grouped(int mode, const uint8_t* a_codes, const uint8
   return cuda_status(launch_gemm(mode, maps, p, grid, stream));
 }
 
+// One CTA whose pipeline wait nobody completes: the bounded mbarrier wait of
+// the kernels gives up after kWaitLimitCycles (about a second) and records
+// kStatusTimeout; the CTA then returns normally.
+__global__ void selftest_wait_timeout_kernel(int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, &abort_flag, status);
+}
+
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -535,6 +550,13 @@ nvfp4_status nvfp4_moe_calibrate(const void* x_calib, int64_t Tc, int64_t H, int
   if (d_amax && cudaMemcpyAsync(d_amax, w.amax, sizeof(float) * E, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
     return NVFP4_ERR_CUDA;
   return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_selftest_wait_timeout(nvfp4_stream_t stream) {
+  const DeviceInfo* dev = device_info();
+  if (!dev) return NVFP4_ERR_NO_DEVICE;
+  selftest_wait_timeout_kernel<<<1, 32, 0, stream>>>(dev->status);
+  return cuda_status(cudaGetLastError());
 }
 
 nvfp4_status nvfp4_device_status(nvfp4_stream_t stream, int32_t* host_out) {
