@@ -440,9 +440,9 @@ namespace {
 struct MoeW16Layout {
   size_t h, dn, total;
 };
-MoeW16Layout moe_w16_layout(int64_t T, int64_t H, int64_t I, int64_t E, int topk) {
+// bf16 h of every route, then the fp32 down rows of every route.
+MoeW16Layout moe_w16_layout(int64_t T, int64_t H, int64_t I, int topk) {
   MoeW16Layout L{};
-  (void)E;
   const int64_t R = T * topk;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -468,7 +468,7 @@ nvfp4_status moe_w16_check(int64_t T, int64_t H, int64_t I, int64_t E, int topk)
 
 size_t nvfp4_moe_w4a16_workspace(int64_t T, int64_t H, int64_t I, int64_t E, int topk) {
   if (moe_w16_check(T, H, I, E, topk) != NVFP4_OK) return 0;
-  return moe_w16_layout(T, H, I, E, topk).total;
+  return moe_w16_layout(T, H, I, topk).total;
 }
 
 nvfp4_status nvfp4_moe_w4a16(const void* x, int64_t T, int64_t H, int64_t I, int64_t E, int topk,
@@ -487,7 +487,7 @@ nvfp4_status nvfp4_moe_w4a16(const void* x, int64_t T, int64_t H, int64_t I, int
       (reinterpret_cast<uintptr_t>(topk_w) & 3u) || (reinterpret_cast<uintptr_t>(d_alpha13) & 3u) ||
       (reinterpret_cast<uintptr_t>(d_alpha2) & 3u))
     return NVFP4_ERR_MISALIGNED;
-  const MoeW16Layout L = moe_w16_layout(T, H, I, E, topk);
+  const MoeW16Layout L = moe_w16_layout(T, H, I, topk);
   if (ws_bytes < L.total) return NVFP4_ERR_WORKSPACE_TOO_SMALL;
   const DeviceInfo* dev = device_info();
   if (!dev) return NVFP4_ERR_NO_DEVICE;
