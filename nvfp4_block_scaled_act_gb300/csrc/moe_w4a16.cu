@@ -13,9 +13,10 @@
 // A slot is an expert in use (ascending expert id); its routes are taken in
 // route order, in passes of 8 (or 16) route rows.  Every CTA derives the slot
 // table from the top-k ids itself (no routing kernel).  Items are dealt
-// round-robin to persistent CTAs; a producer lane streams the weights of the
-// CTA's items through one ring of 128-k blocks (TMA boxes of 64 code bytes
-// per row plus the 128-k block's scale atoms) without stopping between items.
+// round-robin to persistent CTAs; two producer lanes (codes, scales) stream
+// the weights of the CTA's items through one ring of 128-k blocks (TMA boxes
+// of 64 code bytes per row plus the 128-k block's scale atoms) without
+// stopping between items.
 // The compute warps stage the route rows (x or h) in windows of up to 1024 k
 // as f16 after a power-of-two rescale per row and window, multiply with the
 // W4A16 arithmetic of nvfp4_decode.cuh (f16 weights on mma.sync), undo the
