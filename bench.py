@@ -172,6 +172,12 @@ class Workload:
         self.moe_ws = torch.empty(nv.nvfp4_moe_workspace(MOE_T, H, I, E, topk), dtype=torch.uint8, device=dev)
         self.moe_E, self.moe_I, self.moe_H, self.moe_topk = E, I, H, topk
         self.moe_flops = 2.0 * MOE_T * topk * 3 * H * I
+        # algorithmic bytes of the layer: the touched experts' W13 and W2 (codes and
+        # scales), x and out in bf16, and the NVFP4 intermediate written and read once
+        used = int(torch.unique(mc.topk_ids).numel())
+        ebytes = 2 * I * H // 2 + nv.nvfp4_scale_bytes(2 * I, H) + H * I // 2 + nv.nvfp4_scale_bytes(H, I)
+        R = MOE_T * topk
+        self.moe_bytes = used * ebytes + 2 * MOE_T * H * 2 + 2 * (R * I // 2 + nv.nvfp4_scale_bytes(R, I))
         # W4A16 MoE for small batches on the same expert banks (decode-sized T)
         self.moe16_a13 = nv.nvfp4_make_alpha(None, self.moe_W.g13)
         self.moe16_a2 = nv.nvfp4_make_alpha(None, self.moe_W.g2)
@@ -408,7 +414,12 @@ def run_ours(args, world, rank, local):
                       "frac_hbm": round(wl.quant_bytes / t_quant / 1e9 / hbm, 4)},
         "decode": decode,
         "moe": {"ms": round(t_moe * 1e3, 4), "tflops": round(wl.moe_flops / t_moe / 1e12, 1),
-                "frac_fp4_peak": round(wl.moe_flops / t_moe / 1e12 / fp4_peak, 4)},
+                "frac_fp4_peak": round(wl.moe_flops / t_moe / 1e12 / fp4_peak, 4),
+                # the layer's roofline time is the larger of its FP4 and HBM times
+                "bytes": wl.moe_bytes,
+                "roofline_us": round(max(wl.moe_flops / (fp4_peak * 1e12), wl.moe_bytes / (hbm * 1e9)) * 1e6, 1),
+                "roofline_bound": "hbm" if wl.moe_bytes / (hbm * 1e9) > wl.moe_flops / (fp4_peak * 1e12) else "tensor",
+                "frac_roofline": round(max(wl.moe_flops / (fp4_peak * 1e12), wl.moe_bytes / (hbm * 1e9)) / t_moe, 4)},
         "moe_w4a16": moe16,
         # the dominant kernel of the step (about 90 % of its device time, see
         # profiles/launches_bench_step.md) is the decode GEMM; its roofline is
