@@ -7,7 +7,6 @@ import socket
 import sys
 from contextlib import redirect_stdout
 
-import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
