@@ -239,13 +239,16 @@ nvfp4_status nvfp4_moe_calibrate(const void* x_calib_bf16, int64_t Tc, int64_t H
  * result is deterministic (no atomics in the sums).
  * --------------------------------------------------------------------------- */
 
-/* Workspace bytes of nvfp4_moe_w4a16 for T tokens (fp32 gate_up sums and
- * down partials of every route); 0 for an unsupported shape. */
+/* Workspace bytes of nvfp4_moe_w4a16 for T tokens: the bf16 h of every route
+ * [T*topk, I] and its fp32 weighted down row [T*topk, H]; 0 for an
+ * unsupported shape. */
 size_t nvfp4_moe_w4a16_workspace(int64_t T, int64_t H, int64_t I, int64_t E, int topk);
 
-/* gate_up (fp32 G, U per route) -> down (h staged from G, U; routing
- * weight) -> slot sum -> bf16: three kernels chained by programmatic
- * dependent launch.  No host synchronisation. */
+/* gate_up (64 gate rows with the matching 64 up rows per work item, h
+ * written in its epilogue) -> down (w * alpha2 * h @ W2[e].T per route) ->
+ * slot sum -> bf16:
+ * three kernels chained by programmatic dependent launch.  No host
+ * synchronisation. */
 nvfp4_status nvfp4_moe_w4a16(const void* x_bf16, int64_t T, int64_t H, int64_t I, int64_t E, int topk,
                              const int32_t* topk_ids, const float* topk_w, const uint8_t* w13_codes,
                              const uint8_t* w13_sf, const float* d_alpha13, const uint8_t* w2_codes,
