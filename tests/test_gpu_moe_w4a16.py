@@ -164,6 +164,18 @@ def test_moe_w4a16_zero_tokens_and_bad_shapes(nv, small):
     assert nv.nvfp4_moe_w4a16_workspace(4, S["H"], S["I"], S["E"], 9) == 0    # topk > 8
 
 
+@pytest.mark.parametrize("E,topk,T", [(1, 1, 20), (2, 2, 3), (3, 2, 64)])
+def test_moe_w4a16_smallest_shapes(nv, E, topk, T):
+    """H = I = 128 (one 128-k block per GEMV; gate_up items of 64 gate + 64 up
+    rows are the whole expert), every route on one or two experts, and more
+    routes per expert than one pass of route rows holds."""
+    bank = Bank(nv, E, 128, 128, False, eager=True)
+    c = synthdata.moe_case(T, E, 128, 128, topk, False, seed=50 + E, device="cpu")
+    out = bank.gpu(nv, c.x, c.topk_ids, c.topk_w)
+    assert nv.nvfp4_device_status() == 0
+    check_close(out.cpu(), bank.ref(c.x, c.topk_ids, c.topk_w), f"W4A16 MoE E={E} top-{topk} T={T}")
+
+
 @pytest.fixture(scope="module")
 def large(nv):
     return Bank(nv, L["E"], L["H"], L["I"], L["skewed"], eager=False)
