@@ -268,7 +268,10 @@ class Workload:
         self.flush_buf.fill_(1)
 
     def launches_per_step(self) -> int:
-        return (3 + sum(d["ncopy"] * d["launches"] for d in self.decode) + 7 +
+        # prefill (quantise + GEMM), GEMM alone, quantiser alone; the decode graphs;
+        # the W4A4 MoE layer (align x3, quantise/permute, gate_up, down, finalize);
+        # the W4A16 MoE graphs (gate_up, down, finalize per call)
+        return (4 + sum(d["ncopy"] * d["launches"] for d in self.decode) + 7 +
                 3 * len(self.moe16_banks) * len(self.moe16))
 
 
