@@ -231,43 +231,54 @@ __global__ void __launch_bounds__(256) gemv_reduce_kernel(const float* __restric
 // Default decode path.
 //
 // A CTA owns one 128-row block of the weight and a k-range of kc elements; the
-// k-ranges of a row block form one thread-block cluster (at most 8 CTAs), and
-// the cluster sums its partials through distributed shared memory in rank
-// order, so the result is deterministic and no workspace is needed.
+// k-ranges of a row block form one thread-block cluster (at most 8 CTAs).
 //
 // Weight stream.  One producer lane copies the CTA's slice into a ring of
 // shared-memory slots: per 128-k block one TMA tile of codes (64 bytes x 128
 // rows) and its two scale atoms (1 KB, contiguous in the swizzled layout).  As
-// many slots as fit are filled before the kernel waits for the preceding
-// kernel on the stream (programmatic dependent launch), so the weight stream of
-// back-to-back decode calls overlaps the end of the previous call; the
-// producer refills slots as the compute warps release them.
+// many slots as fit are filled, and the blocks beyond them are prefetched into
+// L2, before the kernel waits for the preceding kernel on the stream
+// (programmatic dependent launch); the producer refills slots as the compute
+// warps release them.  A call has one CTA per SM at most (the cluster size is
+// the number of SMs over the row blocks) and a CTA takes under half of an
+// SM's shared memory and registers, so the next call's CTAs are resident
+// while this call computes and their weight copies overlap it.
 //
-// Arithmetic.  Eight compute warps: four row groups of 32 rows x two k
-// parities.  mma.sync.m16n8k16 with 16 weight rows as A and 8 tokens as B
-// (tokens 8..15 in a second MMA), fp32 accumulate.  Inside a 128-k block the
-// k order is permuted so that one 16-byte code load of row r (k = 32t .. 32t+31
-// for lane t) feeds A of that row directly; the activations are staged in the
-// same order.  A code byte becomes an f16x2 pair with one hardware conversion,
-// times the block scale: e2m1 * E4M3 has at most 6 significant bits and lies
-// in [2^-10, 2688], so it is exact in f16.  Activations are bf16; they are
-// staged as f16 after a per-token power-of-two rescale chosen from the
-// token's largest magnitude in the CTA's k-range (that magnitude lands in
-// [2^14, 2^15)): every value within 2^32 of it converts exactly, and the
-// rescale is undone exactly on the fp32 partial sums.  Products of f16 values
-// are exact in fp32.
+// Activations.  After the dependency wait the compute warps stage the CTA's
+// k-range of the T tokens as f16: each (token, 128-k block) is rescaled by its
+// own power of two, which puts its largest magnitude in [2^14, 2^15), so one
+// half-warp finds the block maximum and converts the block with no exchange
+// beyond its own lanes.  A bf16 value within 2^31 of that maximum converts
+// exactly; smaller values round on the f16 subnormal grid, an error below
+// 2^-39 of the maximum.
+//
+// Arithmetic.  Sixteen compute warps: eight 16-row tiles x two k-groups (the
+// 128-k blocks are dealt to the groups round-robin).  mma.sync.m16n8k16 with
+// 16 weight rows as A and 8 tokens as B (tokens 8..15 in a second MMA), each
+// 128-k block into a fresh fp32 accumulator that is then added, times the
+// block's inverse rescale (a power of two, exact), to the running sums.
+// Inside a 128-k block the k order is permuted so that one 16-byte code load
+// of row r (k = 32t .. 32t+31 for lane t) feeds A of that row directly; the
+// activations are staged in the same order.  A code byte becomes an f16x2
+// pair with one hardware conversion, times the block scale: e2m1 * E4M3 has
+// at most 6 significant bits and lies in [2^-10, 2688], so it is exact in
+// f16, and products of f16 values are exact in fp32.
+//
+// Split-K sum.  The two k-groups add their partials in shared memory in a
+// fixed order.  Rank r of the cluster owns rows [r * rows_per, ...) of the
+// row block: every CTA pushes its partials of those rows into the owner's
+// shared memory with st.async, which counts the bytes on the owner's
+// mbarrier; the owner adds the cluster's partials in rank order and writes
+// bf16.  Nobody waits for anything but the bytes it needs, and the result is
+// the same from run to run.
 // ---------------------------------------------------------------------------
-constexpr int kRingRows = 128;                        // weight rows per CTA (one scale-atom row block)
-// Compute warps: 4 row groups x 2 k-groups (128-k blocks dealt round-robin),
-// plus one producer warp.  Small CTAs matter more than more warps: at T <= 8
-// three of them fit an SM's registers, so the next call's CTAs can become
-// resident and start their weight copies while this call still runs (a
-// 12-warp variant lost that and ran 5120x4352 at 10.9 us instead of 7.1 us).
+constexpr int kRingRows = 128;             // weight rows per CTA (one scale-atom row block)
+constexpr int kRingTiles = kRingRows / 16;  // 16-row MMA tiles per CTA
 template <bool kTok16> struct RingShape {
-  static constexpr int kGroups = 2;
-  static constexpr int kCompWarps = 4 * kGroups;
-  static constexpr int kThreads = (kCompWarps + 1) * 32;
-  static constexpr int kMinBlocks = kTok16 ? 2 : 3;  // T <= 16 is held to two by its shared memory
+  static constexpr int kGroups = 2;                         // k-groups
+  static constexpr int kCompWarps = kRingTiles * kGroups;   // one tile per warp
+  static constexpr int kThreads = (kCompWarps + 1) * 32;    // + one producer warp
+  static constexpr int kMinBlocks = 2;
 };
 constexpr int kRingMaxSlots = 24;
 constexpr int kRingChunk = kRingRows * 64;            // codes of one 128-k block
@@ -275,6 +286,23 @@ constexpr int kRingChunkSf = 1024;                    // its two scale atoms
 constexpr int kRingSlot = kRingChunk + kRingChunkSf;
 constexpr int kRingMaxCluster = 8;
 constexpr size_t kRingSmemBudget = 109 * 1024;        // two CTAs per SM with their static shared memory
+constexpr int kStageLoads = 4;                        // activation units in flight per lane while staging
+
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+// Store one fp32 into another CTA's shared memory and count its 4 bytes on
+// that CTA's mbarrier.
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
+               "r"(__float_as_uint(v)), "r"(remote_bar)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 
 template <bool kTok16>
 __global__ void __launch_bounds__(RingShape<kTok16>::kThreads, RingShape<kTok16>::kMinBlocks) gemv_ring_kernel(
@@ -283,16 +311,16 @@ __global__ void __launch_bounds__(RingShape<kTok16>::kThreads, RingShape<kTok16>
     uint16_t* __restrict__ out, int64_t ldo, int* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  __shared__ unsigned int tok_amax[16];
   __shared__ __align__(8) uint64_t full[kRingMaxSlots];
   __shared__ __align__(8) uint64_t empty[kRingMaxSlots];
+  __shared__ __align__(8) uint64_t red_bar;
   __shared__ volatile int abort_flag;
-  pdl_launch_dependents();
 
   constexpr int kGroups = RingShape<kTok16>::kGroups;
-  constexpr int kRingWarps = RingShape<kTok16>::kCompWarps;
+  constexpr int kCompWarps = RingShape<kTok16>::kCompWarps;
+  constexpr int kComp = kCompWarps * 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool producer = (warp == kRingWarps) && lane == 0;
+  const bool producer = (warp == kCompWarps) && lane == 0;
   if (producer) prefetch_tmap(&cmap);
   const uint32_t ncl = cluster_nctarank();
   const uint32_t rank = cluster_ctarank();
@@ -300,23 +328,33 @@ __global__ void __launch_bounds__(RingShape<kTok16>::kThreads, RingShape<kTok16>
   const int k_begin = static_cast<int>(rank) * kc;
   const int k_len = max(0, min(kc, K - k_begin));
   const int nkb = k_len / 128;
-  uint8_t* ring = sm;                                             // R x codes
-  uint8_t* ring_sf = ring + R * kRingChunk;                       // R x scales
+  const int kcb = kc / 128;
+  const int rows_per = (kRingRows + static_cast<int>(ncl) - 1) / static_cast<int>(ncl);
+  const int my_rows = min(rows_per, kRingRows - static_cast<int>(rank) * rows_per);
+  uint8_t* ring = sm;                                                // R x codes
+  uint8_t* ring_sf = ring + R * kRingChunk;                          // R x scales
   const int xs_stride = kc * 2 + 16;
-  uint8_t* xs = ring_sf + R * kRingChunkSf;                       // [T][kc*2+16] f16 activations
-  float* part = reinterpret_cast<float*>(xs + T * xs_stride);     // [T][128] partial sums
+  uint8_t* xs = ring_sf + R * kRingChunkSf;                          // [T][kc] f16 activations, permuted
+  float* xmul = reinterpret_cast<float*>(xs + T * xs_stride);        // [kcb][16] inverse rescales
+  float* part = xmul + kcb * 16;                                     // [T][128] this CTA's partials
+  float* recv = part + T * kRingRows;                                // [ncl][T][rows_per] partials of my rows
   const uint8_t* sf_src = w_sf + (static_cast<int64_t>(rb) * (K / 64) + k_begin / 64) * 512;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int i = 0; i < R; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 4);
+      mbar_init(&empty[i], kRingTiles);
     }
+    mbar_init(&red_bar, 1);
+    // the cluster's pushes of my rows: (ncl - 1) CTAs x T tokens x my_rows fp32
+    mbar_arrive_expect_tx(&red_bar, (ncl - 1) * static_cast<uint32_t>(T * my_rows) * 4u);
     fence_barrier_init();
   }
-  if (threadIdx.x < 16) tok_amax[threadIdx.x] = 0u;
   __syncthreads();
+  // every CTA's red_bar is initialised before anyone pushes (the matching wait
+  // comes after the k-loop)
+  cluster_arrive_relaxed();
   int issued = 0;  // producer: fills issued so far (chunk c goes to slot c % R, phase c / R)
   if (producer) {
     // the weight does not depend on the preceding kernel: fill the ring now
@@ -327,100 +365,23 @@ __global__ void __launch_bounds__(RingShape<kTok16>::kThreads, RingShape<kTok16>
       tma_load_2d(ring + c * kRingChunk, &cmap, &full[c], k_begin / 2 + c * 64, rb * kRingRows);
       bulk_load(ring_sf + c * kRingChunkSf, sf_src + c * kRingChunkSf, kRingChunkSf, &full[c]);
     }
+    // the blocks the ring cannot hold yet go to L2, so that the refills after
+    // the dependency wait read them from there
+    for (int c = pre; c < nkb; ++c) {
+      tma_prefetch_2d(&cmap, k_begin / 2 + c * 64, rb * kRingRows);
+      bulk_prefetch_l2(sf_src + c * kRingChunkSf, kRingChunkSf);
+    }
   }
 
   // activations, alpha and the output follow the preceding kernel
   pdl_wait();
-  const float alpha = __ldg(d_alpha);
-  const int units = k_len / 8;  // 16-byte activation units per token
-  constexpr int kComp = kRingWarps * 32;
-  const int nunits = T * units;
-  if constexpr (kTok16) {
-    if (warp < kRingWarps) {
-      // raw bf16 straight into the permuted slots, every copy in flight at once
-      for (int u = threadIdx.x; u < nunits; u += kComp) {
-        const int tok = u / units;
-        const int k8 = (u - tok * units) * 8;
-        cp_async_16(xs + tok * xs_stride + (k8 >> 7) * 256 + xchunk((k8 & 127) >> 3) * 16,
-                    x + static_cast<int64_t>(tok) * ldx + k_begin + k8);
-      }
-      cp_async_wait_all();
-    }
-    __syncthreads();
-  }
-  if (warp < kRingWarps) {
-    // token amax: the 32 units of a warp span at most three tokens (units is a
-    // multiple of 16); one warp max and one shared atomic per token spanned.
-    // At T <= 8 the units come from global memory in one round of register
-    // loads (up to kXB per thread) and are stored raw into their slots.
-    constexpr int kXB = kTok16 ? 1 : 8;
-    for (int ub0 = threadIdx.x - lane; ub0 < nunits; ub0 += kXB * kComp) {
-      uint4 v[kXB];
-#pragma unroll
-      for (int q = 0; q < kXB; ++q) {
-        const int u = ub0 + q * kComp + lane;
-        v[q] = make_uint4(0u, 0u, 0u, 0u);
-        if (u < nunits) {
-          const int tok = u / units;
-          const int k8 = (u - tok * units) * 8;
-          if constexpr (kTok16)
-            v[q] = *reinterpret_cast<const uint4*>(xs + tok * xs_stride + (k8 >> 7) * 256 +
-                                                   xchunk((k8 & 127) >> 3) * 16);
-          else
-            v[q] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * ldx + k_begin + k8));
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < kXB; ++q) {
-        const int ubase = ub0 + q * kComp;
-        if (ubase >= nunits) break;  // warp-uniform
-        const int u = ubase + lane;
-        const bool in = u < nunits;
-        const int tok = in ? u / units : T;
-        float m = 0.0f;
-        const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          m = fmaxf(m, fabsf(bf16_bits_to_f32(w4[e] & 0xFFFFu)));
-          m = fmaxf(m, fabsf(bf16_bits_to_f32(w4[e] >> 16)));
-        }
-        const int t0 = ubase / units, t1 = min(T - 1, (ubase + 31) / units);
-        for (int tt = t0; tt <= t1; ++tt) {
-          const unsigned int mb = __reduce_max_sync(0xFFFFFFFFu, (in && tok == tt) ? __float_as_uint(m) : 0u);
-          if (lane == 0 && mb != 0u) atomicMax(&tok_amax[tt], mb);
-        }
-        if (!kTok16 && in) {
-          const int k8 = (u - tok * units) * 8;
-          *reinterpret_cast<uint4*>(xs + tok * xs_stride + (k8 >> 7) * 256 + xchunk((k8 & 127) >> 3) * 16) = v[q];
-        }
-      }
-    }
-  }
-  __syncthreads();
-  if (warp < kRingWarps) {
-    // in place: bf16 -> f16 after the token's power-of-two rescale
-    for (int u = threadIdx.x; u < nunits; u += kComp) {
-      const int tok = u / units;
-      const float f = pow2f(-token_shift(tok_amax[tok]));
-      const int k8 = (u - tok * units) * 8;
-      uint4* slot = reinterpret_cast<uint4*>(xs + tok * xs_stride + (k8 >> 7) * 256 + xchunk((k8 & 127) >> 3) * 16);
-      const uint4 v = *slot;
-      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __half2 h =
-            __floats2half2_rn(bf16_bits_to_f32(w4[e] & 0xFFFFu) * f, bf16_bits_to_f32(w4[e] >> 16) * f);
-        o[e] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      *slot = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-  }
-  __syncthreads();
-
+  // the next call may start now: its CTAs fit beside this call's and copy their
+  // weights while this call computes.  Released only here, after the wait, so
+  // that no more than two calls are in flight and the prefetched weights of
+  // the next one are not pushed out of L2 by calls further ahead.
+  pdl_launch_dependents();
   if (producer) {
-    // refill slots as the compute warps release them (after the barriers above,
-    // which the compute warps pass before they consume anything)
+    // refill slots as the compute warps release them
     int s = 0, round = 1;
     for (int c = R; c < nkb; ++c) {
       if (!mbar_wait(&empty[s], (round - 1) & 1, &abort_flag, status)) break;
@@ -433,102 +394,153 @@ __global__ void __launch_bounds__(RingShape<kTok16>::kThreads, RingShape<kTok16>
         ++round;
       }
     }
-  } else if (warp < kRingWarps) {
-    const int g = lane >> 2, t = lane & 3;
-    const int kp = warp >> 2;
-    const int lr0 = (warp & 3) * 32;
-    int sf_off[4], cofs[4];
+  } else if (warp < kCompWarps) {
+    // stage the activations: half-warp h of warp w takes the (token, block)
+    // pairs p = 2w + h, 2w + h + 2 * kCompWarps, ...; lane l16 holds the
+    // 16-byte unit l16 (k = 8 l16 .. 8 l16 + 7) of the block
+    {
+      const int npairs = T * nkb;
+      const int l16 = lane & 15;
+      for (int p0 = warp * 2 + (lane >> 4); p0 - (lane >> 4) < npairs; p0 += kStageLoads * 2 * kCompWarps) {
+        uint4 v[kStageLoads];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int lr = lr0 + 8 * j + g;
-      sf_off[j] = (lr & 31) * 16 + (lr >> 5) * 4 + 2 * (t & 1) + (t >> 1) * 512;
-      cofs[j] = lr * 64 + 16 * t;
-    }
-    int xofs[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) xofs[i] = g * xs_stride + xchunk(4 * t + i) * 16;
-    const bool tok_lo = g < T, tok_hi = g + 8 < T;
-    // acc[a][h][c]: rows lr0 + 16a + g (+8 for c >= 2) x tokens 8h + 2t (+1 for odd c)
-    float acc[2][kTok16 ? 2 : 1][4];
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int h = 0; h < (kTok16 ? 2 : 1); ++h)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[a][h][c] = 0.0f;
-    int s = kp, round = 0;
-    while (s >= R) {
-      s -= R;
-      ++round;
-    }
-    for (int kb = kp; kb < nkb; kb += kGroups) {
-      if (!mbar_wait(&full[s], round & 1, &abort_flag, status)) break;
-      const uint8_t* cs = ring + s * kRingChunk;
-      const uint8_t* ss = ring_sf + s * kRingChunkSf;
-      uint4 cw[4];
-      uint32_t slo[4], shi[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        cw[j] = *reinterpret_cast<const uint4*>(cs + cofs[j]);
-        scale_pair_f16(*reinterpret_cast<const uint16_t*>(ss + sf_off[j]), slo[j], shi[j]);
-      }
-      fence_proxy_async_smem_read();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-      s += kGroups;
-      while (s >= R) {
-        s -= R;
-        ++round;
-      }
-      const uint8_t* xb = xs + kb * 256;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint4 blo = make_uint4(0u, 0u, 0u, 0u), bhi = make_uint4(0u, 0u, 0u, 0u);
-        if (tok_lo) blo = *reinterpret_cast<const uint4*>(xb + xofs[i]);
-        if (kTok16 && tok_hi) bhi = *reinterpret_cast<const uint4*>(xb + xofs[i] + 8 * xs_stride);
-        uint32_t wf[4][4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t word = (i == 0) ? cw[j].x : (i == 1) ? cw[j].y : (i == 2) ? cw[j].z : cw[j].w;
-          const uint32_t m = (i < 2) ? slo[j] : shi[j];
-          e2m1x4_to_f16x2(word, wf[j]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) wf[j][e] = f16x2_mul(wf[j][e], m);
+        for (int q = 0; q < kStageLoads; ++q) {
+          const int p = p0 + q * 2 * kCompWarps;
+          v[q] = make_uint4(0u, 0u, 0u, 0u);
+          if (p < npairs) {
+            const int tok = p / nkb, kb = p - (p / nkb) * nkb;
+            v[q] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * ldx + k_begin + kb * 128 +
+                                                        l16 * 8));
+          }
         }
 #pragma unroll
-        for (int a = 0; a < 2; ++a) {
-          // A: rows g / g+8 of tile a, k pairs (0,1) then (2,3) of code word i
-          mma_f16_16816(acc[a][0], wf[2 * a][0], wf[2 * a + 1][0], wf[2 * a][1], wf[2 * a + 1][1], blo.x, blo.y);
-          mma_f16_16816(acc[a][0], wf[2 * a][2], wf[2 * a + 1][2], wf[2 * a][3], wf[2 * a + 1][3], blo.z, blo.w);
-          if (kTok16) {
-            mma_f16_16816(acc[a][kTok16 ? 1 : 0], wf[2 * a][0], wf[2 * a + 1][0], wf[2 * a][1], wf[2 * a + 1][1],
-                          bhi.x, bhi.y);
-            mma_f16_16816(acc[a][kTok16 ? 1 : 0], wf[2 * a][2], wf[2 * a + 1][2], wf[2 * a][3], wf[2 * a + 1][3],
-                          bhi.z, bhi.w);
+        for (int q = 0; q < kStageLoads; ++q) {
+          const int p = p0 + q * 2 * kCompWarps;
+          if (p - (lane >> 4) >= npairs) break;  // warp-uniform
+          const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+          // largest magnitude: bf16 bit patterns of |x| order like the values
+          uint32_t m = 0u;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) m = max(m, max(w4[e] & 0x7FFFu, (w4[e] >> 16) & 0x7FFFu));
+#pragma unroll
+          for (int o = 1; o < 16; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+          if (p < npairs) {
+            const int tok = p / nkb, kb = p - (p / nkb) * nkb;
+            const int sh = token_shift(m << 16);
+            const float f = pow2f(-sh);
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __half2 h =
+                  __floats2half2_rn(bf16_bits_to_f32(w4[e] & 0xFFFFu) * f, bf16_bits_to_f32(w4[e] >> 16) * f);
+              o[e] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(xs + tok * xs_stride + kb * 256 + xchunk(l16) * 16) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+            if (l16 == 0) xmul[kb * 16 + tok] = pow2f(sh);
           }
         }
       }
     }
-    // partials with the rescale undone, summed over the k-groups in a fixed
-    // order: the last group writes part[tok][row], each lower one adds its own
+    named_barrier_sync(1, kComp);
+
+    const int g = lane >> 2, t = lane & 3;
+    const int kp = warp / kRingTiles;
+    const int r0 = (warp % kRingTiles) * 16 + g, r1 = r0 + 8;
+    const int cofs0 = r0 * 64 + 16 * t, cofs1 = r1 * 64 + 16 * t;
+    const int sf0 = (r0 & 31) * 16 + (r0 >> 5) * 4 + 2 * (t & 1) + (t >> 1) * 512;
+    const int sf1 = (r1 & 31) * 16 + (r1 >> 5) * 4 + 2 * (t & 1) + (t >> 1) * 512;
+    int xofs[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) xofs[i] = g * xs_stride + xchunk(4 * t + i) * 16;
+    const bool tok_lo = g < T, tok_hi = g + 8 < T;
+    constexpr int kH = kTok16 ? 2 : 1;
+    // acc[h][c]: row r0 (c < 2) or r1 (c >= 2) x token 8h + 2t + (c & 1)
+    float acc[kH][4];
+#pragma unroll
+    for (int h = 0; h < kH; ++h)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[h][c] = 0.0f;
+    // chunk kb sits in slot kb % R, phase (kb / R) & 1; R >= kGroups
+    int s = kp;
+    uint32_t ph = 0;
+    const bool refilled = nkb > R;  // slots are released to the producer only then
+    for (int kb = kp; kb < nkb; kb += kGroups) {
+      if (!mbar_test_wait(smem_u32(&full[s]), ph) && !mbar_wait_slow(&full[s], ph, &abort_flag, status)) break;
+      const uint8_t* cs = ring + s * kRingChunk;
+      const uint8_t* ss = ring_sf + s * kRingChunkSf;
+      const uint4 c0 = *reinterpret_cast<const uint4*>(cs + cofs0);
+      const uint4 c1 = *reinterpret_cast<const uint4*>(cs + cofs1);
+      uint32_t slo0, shi0, slo1, shi1;
+      scale_pair_f16(*reinterpret_cast<const uint16_t*>(ss + sf0), slo0, shi0);
+      scale_pair_f16(*reinterpret_cast<const uint16_t*>(ss + sf1), slo1, shi1);
+      if (refilled) {
+        fence_proxy_async_smem_read();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
+      s += kGroups;
+      if (s >= R) {
+        s -= R;
+        ph ^= 1u;
+      }
+      float blk[kH][4];
+#pragma unroll
+      for (int h = 0; h < kH; ++h)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) blk[h][c] = 0.0f;
+      const uint8_t* xb = xs + kb * 256;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t w0 = (i == 0) ? c0.x : (i == 1) ? c0.y : (i == 2) ? c0.z : c0.w;
+        const uint32_t w1 = (i == 0) ? c1.x : (i == 1) ? c1.y : (i == 2) ? c1.z : c1.w;
+        uint32_t a[4], b[4];
+        e2m1x4_to_f16x2(w0, a);
+        e2m1x4_to_f16x2(w1, b);
+        const uint32_t m0 = (i < 2) ? slo0 : shi0, m1 = (i < 2) ? slo1 : shi1;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          a[e] = f16x2_mul(a[e], m0);
+          b[e] = f16x2_mul(b[e], m1);
+        }
+        uint4 xl = make_uint4(0u, 0u, 0u, 0u);
+        if (tok_lo) xl = *reinterpret_cast<const uint4*>(xb + xofs[i]);
+        // A: rows r0 / r1, k pairs (0,1) then (2,3) of code word i
+        mma_f16_16816(blk[0], a[0], b[0], a[1], b[1], xl.x, xl.y);
+        mma_f16_16816(blk[0], a[2], b[2], a[3], b[3], xl.z, xl.w);
+        if constexpr (kTok16) {
+          uint4 xh = make_uint4(0u, 0u, 0u, 0u);
+          if (tok_hi) xh = *reinterpret_cast<const uint4*>(xb + xofs[i] + 8 * xs_stride);
+          mma_f16_16816(blk[kH - 1], a[0], b[0], a[1], b[1], xh.x, xh.y);
+          mma_f16_16816(blk[kH - 1], a[2], b[2], a[3], b[3], xh.z, xh.w);
+        }
+      }
+      // undo the block's rescale (exact) and add to the running sums
+#pragma unroll
+      for (int h = 0; h < kH; ++h) {
+        const float2 mu = *reinterpret_cast<const float2*>(xmul + kb * 16 + 8 * h + 2 * t);
+        acc[h][0] = fmaf(blk[h][0], mu.x, acc[h][0]);
+        acc[h][1] = fmaf(blk[h][1], mu.y, acc[h][1]);
+        acc[h][2] = fmaf(blk[h][2], mu.x, acc[h][2]);
+        acc[h][3] = fmaf(blk[h][3], mu.y, acc[h][3]);
+      }
+    }
+    // the two k-groups' partials, added in a fixed order (group 0 + group 1)
     for (int grp = kGroups - 1; grp >= 0; --grp) {
       if (kp == grp) {
 #pragma unroll
-        for (int a = 0; a < 2; ++a)
+        for (int h = 0; h < kH; ++h)
 #pragma unroll
-          for (int h = 0; h < (kTok16 ? 2 : 1); ++h)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int row = lr0 + a * 16 + g + 8 * (c >> 1);
-              const int tok = h * 8 + 2 * t + (c & 1);
-              if (tok < T) {
-                float* pp = part + tok * kRingRows + row;
-                const float v = acc[a][h][c] * pow2f(token_shift(tok_amax[tok]));
-                *pp = (grp == kGroups - 1) ? v : __fadd_rn(v, *pp);
-              }
+          for (int c = 0; c < 4; ++c) {
+            const int row = (c < 2) ? r0 : r1;
+            const int tok = h * 8 + 2 * t + (c & 1);
+            if (tok < T) {
+              float* pp = part + tok * kRingRows + row;
+              *pp = (grp == kGroups - 1) ? acc[h][c] : __fadd_rn(acc[h][c], *pp);
             }
+          }
       }
-      if (grp > 0) named_barrier_sync(1, kComp);
+      if (grp > 0) named_barrier_sync(2, kComp);
     }
   }
   __syncthreads();
@@ -542,65 +554,89 @@ __global__ void __launch_bounds__(RingShape<kTok16>::kThreads, RingShape<kTok16>
       }
     }
   }
-  // rank r sums rows [r * rows_per, ...) of the cluster's partials in rank order
-  cluster_arrive();
+  // split-K sum: push the partials of every owner's rows to it, in place
+  // [rank][tok][row - owner's first row] of its receive buffer
   cluster_wait();
-  const int rows_per = (kRingRows + static_cast<int>(ncl) - 1) / static_cast<int>(ncl);
-  for (int e = threadIdx.x; e < T * rows_per; e += blockDim.x) {
-    const int tok = e / rows_per;
-    const int row = static_cast<int>(rank) * rows_per + (e - tok * rows_per);
-    if (row >= kRingRows) continue;
-    float v[kRingMaxCluster];
-#pragma unroll
-    for (int q = 0; q < kRingMaxCluster; ++q)
-      v[q] = q < static_cast<int>(ncl) ? ld_cluster_f32(part + tok * kRingRows + row, q) : 0.0f;
-    float sum = 0.0f;
-#pragma unroll
-    for (int q = 0; q < kRingMaxCluster; ++q) sum += v[q];
-    const int n = rb * kRingRows + row;
-    if (n < N) out[static_cast<int64_t>(tok) * ldo + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum * alpha));
+  const uint32_t recv_local = smem_u32(recv);
+  const uint32_t bar_local = smem_u32(&red_bar);
+  for (int e = threadIdx.x; e < T * kRingRows; e += blockDim.x) {
+    const int tok = e / kRingRows, row = e - (e / kRingRows) * kRingRows;
+    const int owner = row / rows_per;
+    const int idx = (static_cast<int>(rank) * T + tok) * rows_per + (row - owner * rows_per);
+    const float v = part[e];
+    if (owner == static_cast<int>(rank))
+      recv[idx] = v;
+    else
+      st_async_f32(mapa_u32(recv_local + idx * 4, owner), v, mapa_u32(bar_local, owner));
   }
-  cluster_arrive();
-  cluster_wait();
+  __syncthreads();  // my own contribution is in recv
+  // wait for the cluster's pushes of my rows, not cut short by an abort, so
+  // that no push lands after this CTA has exited
+  bool got = false;
+  {
+    const long long t0 = clock64();
+    while (!(got = mbar_try_wait(bar_local, 0)) && clock64() - t0 < 2 * kWaitLimitCycles) {
+    }
+    if (!got && threadIdx.x == 0) record_status(status, kStatusTimeout);
+  }
+  if (got) {
+    const float alpha = __ldg(d_alpha);
+    for (int e = threadIdx.x; e < T * my_rows; e += blockDim.x) {
+      const int tok = e / my_rows, rl = e - (e / my_rows) * my_rows;
+      float sum = 0.0f;
+      for (int q = 0; q < static_cast<int>(ncl); ++q) sum += recv[(q * T + tok) * rows_per + rl];
+      const int n = rb * kRingRows + static_cast<int>(rank) * rows_per + rl;
+      if (n < N) out[static_cast<int64_t>(tok) * ldo + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum * alpha));
+    }
+  }
 }
 
 GemvRingPlan gemv_ring_plan(int64_t T, int64_t N, int64_t K, int num_sms) {
   GemvRingPlan p{};
   const int64_t row_blocks = (N + kRingRows - 1) / kRingRows;
   const int64_t kblocks = K / 128;
-  int64_t cl = (2 * static_cast<int64_t>(num_sms)) / row_blocks;
+  // one CTA per SM: the next call's CTAs fit beside this call's and start
+  // their weight copies while this call computes.  More k-splits only when
+  // the activations of a CTA leave too little room for the ring.
+  int64_t cl = static_cast<int64_t>(num_sms) / row_blocks;
   cl = cl < 1 ? 1 : (cl > kRingMaxCluster ? kRingMaxCluster : cl);
   if (cl > kblocks) cl = kblocks;
-  const int64_t kcb = (kblocks + cl - 1) / cl;
-  p.cl = static_cast<int>(cl);
-  p.kc = static_cast<int>(kcb * 128);
-  p.row_blocks = row_blocks;
-  const size_t fixed = static_cast<size_t>(T) * (kcb * 256 + 16) + static_cast<size_t>(T * kRingRows * 4);
-  int64_t slots = fixed < kRingSmemBudget ? static_cast<int64_t>((kRingSmemBudget - fixed) / kRingSlot) : 0;
-  if (slots > kcb) slots = kcb;
-  if (slots > kRingMaxSlots) slots = kRingMaxSlots;
-  // a ring that is refilled is even: each slot then stays with one k-group
-  // (kb and kb + R have the same parity), so no warp waits on a slot two
-  // phases ahead of the last one it read, where the mbarrier parity test
-  // would pass on a stale phase
-  if (slots < kcb && slots > 1) slots &= ~int64_t{1};
-  p.R = static_cast<int>(slots);
-  p.ok = slots >= 2 || (slots >= 1 && kcb == 1);
-  p.smem = fixed + static_cast<size_t>(slots) * kRingSlot + 1024;  // + alignment slack
-  return p;
+  for (;; ++cl) {
+    const int64_t kcb = (kblocks + cl - 1) / cl;
+    const int64_t ncl = (kblocks + kcb - 1) / kcb;  // no CTA without k-blocks
+    const int64_t rows_per = (kRingRows + ncl - 1) / ncl;
+    // activations, inverse rescales, partials and the receive buffer
+    const size_t fixed = static_cast<size_t>(T) * (kcb * 256 + 16) + static_cast<size_t>(kcb * 16 * 4) +
+                         static_cast<size_t>(T * kRingRows * 4) + static_cast<size_t>(ncl * T * rows_per * 4);
+    int64_t slots = fixed < kRingSmemBudget ? static_cast<int64_t>((kRingSmemBudget - fixed) / kRingSlot) : 0;
+    if (slots > kcb) slots = kcb;
+    if (slots > kRingMaxSlots) slots = kRingMaxSlots;
+    // a ring that is refilled is even: each slot then stays with one k-group
+    // (kb and kb + R have the same parity), so no warp waits on a slot two
+    // phases ahead of the last one it read, where the mbarrier parity test
+    // would pass on a stale phase
+    if (slots < kcb && slots > 1) slots &= ~int64_t{1};
+    const bool ok = slots >= 2 || (slots >= 1 && kcb == 1);
+    const bool roomy = slots >= kcb || slots >= 4;
+    if ((ok && roomy) || cl >= kRingMaxCluster || cl >= kblocks) {
+      p.cl = static_cast<int>(ncl);
+      p.kc = static_cast<int>(kcb * 128);
+      p.row_blocks = row_blocks;
+      p.R = static_cast<int>(slots);
+      p.ok = ok;
+      p.smem = fixed + static_cast<size_t>(slots) * kRingSlot + 1024;  // + alignment slack
+      return p;
+    }
+  }
 }
 
 template <bool kTok16>
 static cudaError_t launch_ring_t(const CUtensorMap& cmap, const void* x, int64_t T, int64_t ldx, const uint8_t* w_sf,
                                  int64_t N, int64_t K, const float* d_alpha, void* out, int64_t ldo,
                                  const GemvRingPlan& plan, int* status, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_ring_kernel<kTok16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kRingSmemBudget + 1024));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = cudaFuncSetAttribute(gemv_ring_kernel<kTok16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kRingSmemBudget + 1024));
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(plan.row_blocks * plan.cl));
   cfg.blockDim = dim3(RingShape<kTok16>::kThreads);

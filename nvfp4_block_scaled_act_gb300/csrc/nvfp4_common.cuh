@@ -93,6 +93,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// The waiting part of mbar_wait, kept out of line so that a hot loop carries
+// only the one-instruction test of its fast path.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status) {
+  const uint32_t a = smem_u32(bar);
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      *abort_flag = 1;
+      record_status(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
 // Warp-collective form of mbar_wait: every lane of a converged warp calls it and
 // all get the same answer, so the caller's loop state stays warp-uniform (the
 // addresses, coordinates and descriptors that one lane then hands to TMA or
@@ -139,6 +155,16 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
           smem_u32(smem_dst)),
       "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// L2 prefetches: a 2D tile of a tensor map, and an untiled range (address
+// 16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
 }
 
 // Programmatic dependent launch: a kernel launched with the programmatic

@@ -2,10 +2,12 @@
 // MoE): e2m1 codes times their E4M3 block scale become f16 weights, which
 // enter mma.sync.m16n8k16 as the A operand (16 weight rows) against up to 8
 // activation rows as B; activations are staged as f16 after a power-of-two
-// rescale per row.  e2m1 * E4M3 has at most 6 significant bits and lies in
-// [2^-10, 2688], so the weights are exact in f16, every activation within 2^32
-// of its row's largest magnitude converts exactly, and products of f16 values
-// are exact in the fp32 accumulators.
+// rescale that puts the largest magnitude of the rescaled group in
+// [2^14, 2^15).  e2m1 * E4M3 has at most 6 significant bits and lies in
+// [2^-10, 2688], so the weights are exact in f16; an activation within 2^31 of
+// its group's largest magnitude converts exactly (smaller ones round on the
+// f16 subnormal grid, an error below 2^-39 of that magnitude); and products of
+// f16 values are exact in the fp32 accumulators.
 #pragma once
 #include <cuda_fp16.h>
 

@@ -144,6 +144,29 @@ def test_w4a16_ragged(nv, T, N, K):
         assert torch.equal(again, out), f"W4A16 {T}x{N}x{K} is not repeatable"
 
 
+@pytest.mark.parametrize("T,N,K", [(1, 8704, 5120), (8, 1024, 2048), (16, 640, 4352)])
+def test_w4a16_blocks_of_distant_magnitudes(nv, T, N, K):
+    """Activations whose 128-k blocks differ in magnitude by up to 2^120, with
+    all-zero blocks and blocks holding one nonzero value: the decode kernel
+    rescales each (token, 128-k block) on its own, and the result must still
+    meet the tolerance against the oracle."""
+    case = synthdata.decode_case(T, N, K, seed=77 + T)
+    g = torch.Generator().manual_seed(1234 + T)
+    nb = K // 128
+    exps = torch.randint(-60, 61, (T, nb), generator=g).double()
+    scale = torch.pow(2.0, exps).repeat_interleave(128, dim=1)
+    x = (case.x.double() * scale)
+    zero = torch.rand(T, nb, generator=g) < 0.15
+    x = x.view(T, nb, 128)
+    x[zero] = 0.0
+    lone = torch.rand(T, nb, generator=g) < 0.1
+    x[lone, 1:] = 0.0
+    case.x = x.view(T, K).to(torch.bfloat16)
+    L = Linear(nv, case, quant_act=False)
+    out = nv.nvfp4_linear_w4a16(L.x_dev, L.W.codes, L.W.scales, L.alpha16_dev, N, K)
+    check_close(out, oracle.linear_w4a16(L.x, L.wc, L.ws, N, K, L.alpha16), f"W4A16 distant blocks {T}x{N}x{K}")
+
+
 def test_w4a16_row_strided_and_deterministic(nv):
     T, N, K = 8, 1024, 2048
     L = Linear(nv, synthdata.decode_case(T, N, K, seed=9), quant_act=False)
