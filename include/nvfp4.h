@@ -166,6 +166,8 @@ nvfp4_status nvfp4_linear_w4a16(const void* x_bf16, int64_t T, int64_t ldx,
  *     NVFP4_ERR_WORKSPACE_TOO_SMALL; both decode shapes of the workloads fit.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is kept for the life of the process: a cudaDeviceReset
+ *     after that first call is not supported.
  *   - Every call shares the one array and it keeps the last call's partials;
  *     nothing in it needs to start at zero (each partial is written before it
  *     is read).  Calls that overlap on the GPU (other streams, other threads)

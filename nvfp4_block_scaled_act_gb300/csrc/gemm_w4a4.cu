@@ -934,13 +934,11 @@ using DownCfg = GemmCfg<128, 2, 4, kEpiDownSum>;
 
 template <class Cfg>
 static cudaError_t launch_cfg(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_nvfp4_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // set on every launch: the attribute belongs to the current device, and a
+  // process may launch on several
+  cudaError_t e = cudaFuncSetAttribute(gemm_nvfp4_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   gemm_nvfp4_kernel<Cfg><<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(maps.a, maps.b, p);
   return cudaGetLastError();
 }
@@ -948,13 +946,9 @@ static cudaError_t launch_cfg(const GemmMaps& maps, const GemmParams& p, int gri
 cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {
   switch (mode) {
     case kEpiDense: {
-      static bool attr_set = false;
-      if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             PairCfg::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-      }
+      cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           PairCfg::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
       if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;  // whole CTA pairs
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>(grid));

@@ -683,12 +683,10 @@ static cudaError_t launch_gemv_t(const void* x, int64_t T, int64_t ldx, const ui
                                  const GemvPlan& plan, cudaStream_t stream) {
   constexpr int kTokRows = kTok16 ? 16 : 8;
   const size_t smem = static_cast<size_t>(kTokRows) * (plan.kc * 2 + 64) + 2 * (plan.kc / 64) * 512;
-  static size_t attr = 0;
-  if (smem > 48 * 1024 && smem > attr) {
+  if (smem > 48 * 1024) {  // the attribute belongs to the current device: set it on every launch
     cudaError_t e = cudaFuncSetAttribute(gemv_w4a16_kernel<kTok16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    attr = smem;
   }
   dim3 grid(plan.row_blocks, plan.splits);
   gemv_w4a16_kernel<kTok16><<<grid, 256, smem, stream>>>(static_cast<const uint16_t*>(x), static_cast<int>(T), ldx,

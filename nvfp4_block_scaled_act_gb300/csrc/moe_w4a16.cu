@@ -498,13 +498,10 @@ Moe16Plan moe16_plan(int mode, int64_t K, int64_t T, int64_t E, int topk, int64_
 template <int MODE, bool kTok16>
 static cudaError_t launch_stage(const CUtensorMap& map, const MoeW16Params& p, const Moe16Plan& pl,
                                 cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(moe16_gemv_kernel<MODE, kTok16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kM16SmemBudget + 1024));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // the attribute belongs to the current device: set it on every launch
+  cudaError_t e = cudaFuncSetAttribute(moe16_gemv_kernel<MODE, kTok16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kM16SmemBudget + 1024));
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas));
   cfg.blockDim = dim3(kM16Threads);

@@ -54,6 +54,7 @@ _SIGS = {
     "nvo_moe_w4a4": (None, [_P, _I64, _I64, _I64, _I64, _I64, _P, _P, _F, _P, _P, _P,
                              _F, _P, _P, _P, _P, _P, _P]),
     "nvo_moe_h_amax": (None, [_P, _I64, _I64, _I64, _I64, _F, _P, _P, _P, _P]),
+    "nvo_moe_down": (None, [_P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P]),
     "nvo_moe_w4a16": (None, [_P, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P,
                               _P, _P]),
 }
@@ -233,6 +234,21 @@ def moe_w4a4(x, topk_ids, topk_w, g_a1, w13_codes, w13_sf, alpha13, g_a2, w2_cod
                        _ptr(out), _ptr(hc) if want_h else None, _ptr(hs) if want_h else None)
     out = out.view(torch.bfloat16)
     return (out, hc, hs) if want_h else out
+
+
+def moe_down(h_codes, h_sf, topk_ids, topk_w, w2_codes, w2_sf, alpha2, E, H, I) -> torch.Tensor:
+    """The MoE down projection on a given NVFP4 intermediate: h_codes
+    [T * topk, I/2] and h_sf (swizzled over T * topk rows) hold route
+    t * topk + slot; returns bf16 [T, H] (the layer's last two steps)."""
+    T, topk = topk_ids.shape
+    ids = topk_ids.to(torch.int32).contiguous()
+    w = topk_w.to(torch.float32).contiguous()
+    a2 = torch.as_tensor(alpha2, dtype=torch.float32).contiguous()
+    assert h_codes.shape == (T * topk, I // 2) and h_sf.numel() >= scale_bytes(T * topk, I)
+    out = _bf16_out((T, H))
+    lib().nvo_moe_down(_ptr(h_codes.contiguous()), _ptr(h_sf.contiguous()), T, H, I, E, topk, _ptr(ids),
+                       _ptr(w), _ptr(w2_codes.contiguous()), _ptr(w2_sf.contiguous()), _ptr(a2), _ptr(out))
+    return out.view(torch.bfloat16)
 
 
 def moe_w4a16(x, topk_ids, topk_w, w13_codes, w13_sf, alpha13, w2_codes, w2_sf, alpha2, E, H, I,

@@ -473,6 +473,61 @@ void nvo_moe_w4a4(const uint16_t* x, int64_t T, int64_t H, int64_t I, int64_t E,
 }
 
 /* ------------------------------------------------------------------------- */
+/* MoE down projection on a given NVFP4 intermediate ([moe] "Changes": the     */
+/* routed down GEMM applies the routing weight and sums the top-k outputs).    */
+/* Steps 5 and 6 of the layer above, taken on their own so that a caller can   */
+/* hand in another implementation's h:                                         */
+/*   d[n]   = alpha2[e] * sum_k h^[i,k] * W2^[e][n,k]   fp32, ascending k       */
+/*   y[t,n] = sum over slots s in order of w[t,s] * d[n] (fp32), out = bf16(y)  */
+/* h_codes [T*topk, I/2] and h_sf (swizzled over T*topk rows) hold route       */
+/* i = t * topk + s; routes with an id outside [0, E) are dropped.              */
+/* ------------------------------------------------------------------------- */
+
+void nvo_moe_down(const uint8_t* h_codes, const uint8_t* h_sf, int64_t T, int64_t H, int64_t I,
+                  int64_t E, int64_t topk, const int32_t* topk_ids, const float* topk_w,
+                  const uint8_t* w2_codes, const uint8_t* w2_sf, const float* alpha2, uint16_t* out) {
+  const int64_t R = T * topk;
+  float* Hd = (float*)malloc(sizeof(float) * (size_t)(R * I + 1));
+  nvo_dequant(h_codes, h_sf, R, I, Hd);
+  float* D = (float*)calloc((size_t)(R * H + 1), sizeof(float));
+  float* W2 = (float*)malloc(sizeof(float) * (size_t)(H * I + 1));
+  const size_t w2_bytes = (size_t)H * (size_t)(I / 2), w2_sfb = nvo_scale_bytes(H, I);
+  int64_t* routes = (int64_t*)malloc(sizeof(int64_t) * (size_t)(R + 1));
+  for (int64_t e = 0; e < E; ++e) {
+    int64_t nr = 0;
+    for (int64_t i = 0; i < R; ++i)
+      if (topk_ids[i] == e) routes[nr++] = i;
+    if (nr == 0) continue;
+    nvo_dequant(w2_codes + (size_t)e * w2_bytes, w2_sf + (size_t)e * w2_sfb, H, I, W2);
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t q = 0; q < nr; ++q) {
+      const int64_t i = routes[q];
+      for (int64_t n = 0; n < H; ++n) {
+        float acc = 0.0f;
+        for (int64_t k = 0; k < I; ++k) acc += Hd[i * I + k] * W2[n * I + k];
+        D[i * H + n] = alpha2[e] * acc;
+      }
+    }
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t n = 0; n < H; ++n) {
+      float y = 0.0f;
+      for (int64_t s = 0; s < topk; ++s) {
+        const int64_t i = t * topk + s;
+        const int32_t e = topk_ids[i];
+        if (e < 0 || e >= E) continue;
+        y += topk_w[i] * D[i * H + n];
+      }
+      out[t * H + n] = nvo_f32_to_bf16(y);
+    }
+  free(routes);
+  free(W2);
+  free(D);
+  free(Hd);
+}
+
+/* ------------------------------------------------------------------------- */
 /* W4A16 MoE for small batches ([moe] "Changes": prefill runs W4A4 from 4     */
 /* tokens per expert and W4A16 below; "Decode ... and W4A16 prefill are       */
 /* untouched").  READING: [moe]'s layer with the activations never quantised   */

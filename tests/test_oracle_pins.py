@@ -444,6 +444,54 @@ def test_moe_reduces_to_quantised_mlp():
         assert np.all(err <= 2 * bf16_ulp(np.abs(ref).max()))
 
 
+@pytest.mark.parametrize("topk,seed", [(1, 21), (3, 22)])
+def test_moe_down_matches_fp64_brute_force(topk, seed):
+    """The down stage on an arbitrary NVFP4 intermediate (random codes and
+    scales, as another implementation's h would be): per route
+    d = alpha2[e] * h^ @ W2^[e].T, then the routing-weighted sum over the slots,
+    against an fp64 brute force with independent decoders; a route with an id
+    outside [0, E) contributes nothing."""
+    E, H, I, T = 3, 48, 64, 5
+    d = _tiny_moe(E=E, T=T, topk=topk, seed=seed, H=H, I=I)
+    case = d["case"]
+    rng = np.random.default_rng(seed)
+    R = T * topk
+    hc, hs = _random_nvfp4(R, I, rng)
+    ids = case.topk_ids.clone()
+    ids[2, topk - 1] = -1
+    ids[4, 0] = E
+    got = bf16_np(oracle.moe_down(hc, hs, ids, case.topk_w, d["w2c"], d["w2s"], d["a2"], E, H, I))
+    Hq = dequant_np(hc, hs, R, I)
+    sb = oracle.scale_bytes(H, I)
+    ref = np.zeros((T, H))
+    bound = np.zeros((T, H))
+    for t in range(T):
+        for s in range(topk):
+            e = int(ids[t, s])
+            if e < 0 or e >= E:
+                continue
+            W2 = dequant_np(d["w2c"][e * H:(e + 1) * H], d["w2s"][e * sb:(e + 1) * sb], H, I)
+            i = t * topk + s
+            w = np.float64(np.float32(case.topk_w[t, s]))
+            a2 = np.float64(np.float32(d["a2"][e]))
+            ref[t] += w * a2 * (Hq[i] @ W2.T)
+            # fp32 dot (I terms), times alpha2 and w, then a sum of up to topk terms
+            bound[t] += w * a2 * (I + 3 + topk) * 2.0 ** -24 * (np.abs(Hq[i]) @ np.abs(W2).T)
+    tol = bf16_ulp(ref) * 0.5 + bound * 1.01 + 1e-30
+    assert np.all(np.abs(got - ref) <= tol + bf16_ulp(ref) * 1e-3)
+
+
+def test_moe_down_reproduces_the_layer_on_its_own_intermediate():
+    """Fed the oracle layer's own NVFP4 h, the down stage gives the layer's output
+    bit for bit (the two are the same steps on the same values)."""
+    d = _tiny_moe(E=4, T=7, topk=3, seed=23, H=64, I=32)
+    case, E, H, I = d["case"], d["E"], d["H"], d["I"]
+    out, hc, hs = oracle.moe_w4a4(case.x, case.topk_ids, case.topk_w, d["g_a1"], d["w13c"], d["w13s"], d["a13"],
+                                  d["g_a2"], d["w2c"], d["w2s"], d["a2"], E, H, I, want_h=True)
+    again = oracle.moe_down(hc, hs, case.topk_ids, case.topk_w, d["w2c"], d["w2s"], d["a2"], E, H, I)
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+
+
 def test_moe_identical_experts_ignore_routing():
     d = _tiny_moe(E=4, T=6, topk=3, seed=5, same_experts=True)
     case, E, H, I = d["case"], d["E"], d["H"], d["I"]

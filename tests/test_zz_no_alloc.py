@@ -5,16 +5,18 @@ decode GEMM (a runtime that owns the whole GPU through its own pool, code
 already inside CUDA stream capture, a plugin host that hands out only inputs
 and outputs): it keeps its split-K partials in a 6 MiB array compiled into the
 library instead of a workspace.  Here it is called through the C ABI, twice in
-a row, and compared with the workspace entry point nvfp4_linear_w4a16 within
-the tolerance of the other GEMM tests.  Shapes whose partials exceed the array
-are refused.  This file is collected last so that a stop at the first failure
-has already run every other test; it also passes alone in a fresh process.
+a row, and each result is compared element by element with the oracle within
+the tolerance of the other GEMM tests (and, as a second check, with the
+workspace entry point).  Shapes whose partials exceed the array are refused.
+This file is collected last so that a stop at the first failure has already
+run every other test; it also passes alone in a fresh process.
 """
 import ctypes
 
 import pytest
 import torch
 
+import oracle
 import synthdata
 from parity import check_close
 
@@ -44,25 +46,34 @@ def _call_noalloc(lib, x, W, alpha, N, K, out):
 
 
 @pytest.mark.parametrize("T,N,K", [(16, 8704, 5120), (1, 5120, 4352), (5, 1032, 256), (16, 5120, 4352)])
-def test_noalloc_matches_workspace_entry_point(nv, T, N, K):
+def test_noalloc_matches_oracle(nv, T, N, K):
     case = synthdata.decode_case(T, N, K, seed=T + N)
-    W = nv.quantize_weight(case.w_parts[0].to(DEV))
+    w = case.w_parts[0]
+    W = nv.quantize_weight(w.to(DEV))
+    wc, ws = oracle.quantize(w, oracle.global_scale(w))
+    assert torch.equal(W.codes.cpu(), wc) and torch.equal(W.scales.cpu(), ws)
     alpha = nv.nvfp4_make_alpha(None, W.g)
+    ref = oracle.linear_w4a16(case.x, wc, ws, N, K, oracle.alpha_w4a16(oracle.global_scale(w)))
     x = case.x.to(DEV)
-    ref = nv.nvfp4_linear_w4a16(x, W.codes, W.scales, alpha, N, K)
     lib = nv.load_library()
     for _ in range(2):  # two calls in a row share the static array
         out = torch.full((T, N), float("nan"), dtype=torch.bfloat16, device=DEV)
         assert _call_noalloc(lib, x, W, alpha, N, K, out) == 0
         torch.cuda.synchronize()
-        check_close(out, ref, f"no-alloc W4A16 {T}x{N}x{K}")
+        check_close(out, ref, f"no-alloc W4A16 {T}x{N}x{K} against the oracle")
+        check_close(out, nv.nvfp4_linear_w4a16(x, W.codes, W.scales, alpha, N, K),
+                    f"no-alloc W4A16 {T}x{N}x{K} against the workspace entry point")
     assert nv.nvfp4_device_status() == 0
 
 
 def test_noalloc_refuses_shapes_beyond_its_array(nv):
-    # 100 blocks of 256 rows on 152 SMs give 4 k-splits: 4 * 16 * 25600 fp32
-    # partials = 6.25 MiB, more than the 6 MiB array
-    T, N, K = 16, 25600, 4096
+    """2 * SMs - 1 blocks of 256 rows split K in two: 2 * 16 * N fp32 partials,
+    about SMs * 64 KB, more than the 6 MiB array on any GPU with 100 or more
+    SMs (the shape follows the SM count torch reports)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert sms >= 100
+    T, N, K = 16, (2 * sms - 1) * 256, 256
+    assert 2 * T * N * 4 > 6 * 1024 * 1024
     x = torch.zeros(T, K, dtype=torch.bfloat16, device=DEV)
     codes = torch.zeros(N, K // 2, dtype=torch.uint8, device=DEV)
     scales = torch.zeros(nv.nvfp4_scale_bytes(N, K), dtype=torch.uint8, device=DEV)
