@@ -196,6 +196,20 @@ class Workload:
         self.flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
 
+    def large_moe(self):
+        """Weights and static globals of the E = 256 MoE (built on first use):
+        (W, g_a1, alpha13, g_a2, alpha2)."""
+        nv = self.nv
+        cfg = synthdata.MOE_LARGE
+        E, H, I, topk = cfg["E"], cfg["H"], cfg["I"], cfg["topk"]
+        mc = synthdata.moe_case(16, E, H, I, topk, cfg["skewed"], seed=0, device=self.dev)
+        W = nv.quantize_moe_weights(lambda e: mc.w13(e), lambda e: mc.w2(e), E, H, I, self.dev)
+        g1 = nv.nvfp4_compute_global(mc.x_calib)
+        a13 = nv.nvfp4_make_alpha(g1, W.g13)
+        g2, _ = nv.nvfp4_moe_calibrate(mc.x_calib, g1, W.w13_codes, W.w13_sf, a13, E, I)
+        a2 = nv.nvfp4_make_alpha(g2, W.g2)
+        return W, g1, a13, g2, a2
+
     # --- stages ------------------------------------------------------------
     def prefill(self):
         nv = self.nv
@@ -316,6 +330,111 @@ def _timed(fn, stream):
     return a, b
 
 
+def _median_ms(fn, flush, reps, stream):
+    """Median CUDA-event time of fn over reps runs, the L2 flushed before each
+    (outside the events)."""
+    ts = []
+    for _ in range(reps):
+        flush()
+        a, b = _timed(fn, stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def _roof(flops, nbytes, seconds, hbm, fp4_peak):
+    """Achieved rates and the roofline of one timed stage: the roofline time is
+    the larger of its FP4 tensor time and its HBM time."""
+    t_fp4 = flops / (fp4_peak * 1e12)
+    t_hbm = nbytes / (hbm * 1e9)
+    return {"tflops": round(flops / seconds / 1e12, 2), "gbs": round(nbytes / seconds / 1e9, 1),
+            "frac_fp4_peak": round(flops / seconds / 1e12 / fp4_peak, 4),
+            "bytes": int(nbytes), "roofline_us": round(max(t_fp4, t_hbm) * 1e6, 2),
+            "bound": "tensor" if t_fp4 >= t_hbm else "hbm",
+            "frac_roofline": round(max(t_fp4, t_hbm) / seconds, 4)}
+
+
+def _moe_bytes(nv, ids, T, E, H, I, topk):
+    """Algorithmic bytes of one MoE layer: the W13 and W2 codes and scales of the
+    experts in use, x and out in bf16, the NVFP4 intermediate written and read once."""
+    used = int(torch.unique(ids[(ids >= 0) & (ids < E)]).numel())
+    ebytes = 2 * I * H // 2 + nv.nvfp4_scale_bytes(2 * I, H) + H * I // 2 + nv.nvfp4_scale_bytes(H, I)
+    R = T * topk
+    return used * ebytes + 2 * T * H * 2 + 2 * (R * I // 2 + nv.nvfp4_scale_bytes(R, I)), used
+
+
+def sweep_configs(wl, nv, dev, hbm, fp4_peak, reps=5):
+    """Every workload shape, timed stage by stage outside the step (each the
+    median of `reps` runs, L2 flushed before each): the tiny W4A4 linear, the
+    fused-qkv prefill at every M (quantise + GEMM, and the GEMM alone), the
+    E = 128 MoE layer at every T and the E = 256 MoE layer at every T."""
+    stream = torch.cuda.current_stream()
+    flush = wl.flush
+    out = {}
+    # tiny W4A4 linear: M = 8, N = 256, K = 512
+    tc = synthdata.tiny_linear(seed=0, device=dev)
+    Wt = nv.quantize_weight(tc.w_parts)
+    gt = nv.nvfp4_compute_global(tc.x_calib)
+    at = nv.nvfp4_make_alpha(gt, Wt.g)
+    ct, st = nv.nvfp4_quantize_act(tc.x, gt)
+    ot = torch.empty(tc.x.shape[0], Wt.N, dtype=torch.bfloat16, device=dev)
+    M, N, K = tc.x.shape[0], Wt.N, Wt.K
+
+    def tiny():
+        nv.nvfp4_quantize_act(tc.x, gt, ct, st)
+        nv.nvfp4_linear_w4a4(ct, st, Wt.codes, Wt.scales, at, N, K, out=ot)
+    t = _median_ms(tiny, flush, 4 * reps, stream) * 1e-3
+    nb = N * K // 2 + nv.nvfp4_scale_bytes(N, K) + 2 * M * K + 2 * M * N
+    out["tiny_w4a4_M8_N256_K512"] = dict(us=round(t * 1e6, 2), **_roof(2.0 * M * N * K, nb, t, hbm, fp4_peak))
+    # prefill, fused qkv weight, every M: rows and scale atoms of the M = 8192
+    # buffers are prefixes of the smaller problems
+    pre = {}
+    N, K = wl.pre_W.N, wl.pre_W.K
+    for M in synthdata.PREFILL_M:
+        x = wl.pre_x[:M]
+        codes, sf = wl.pre_codes[:M], wl.pre_sf[:nv.nvfp4_scale_bytes(M, K)]
+        o = wl.pre_out[:M]
+
+        def quant_gemm(x=x, codes=codes, sf=sf, o=o):
+            nv.nvfp4_quantize_act(x, wl.pre_g, codes, sf)
+            nv.nvfp4_linear_w4a4(codes, sf, wl.pre_W.codes, wl.pre_W.scales, wl.pre_alpha, N, K, out=o)
+
+        def gemm(codes=codes, sf=sf, o=o):
+            nv.nvfp4_linear_w4a4(codes, sf, wl.pre_W.codes, wl.pre_W.scales, wl.pre_alpha, N, K, out=o)
+        tq = _median_ms(quant_gemm, flush, reps, stream) * 1e-3
+        tg = _median_ms(gemm, flush, reps, stream) * 1e-3
+        fl = 2.0 * M * N * K
+        b_gemm = N * K // 2 + nv.nvfp4_scale_bytes(N, K) + M * K // 2 + nv.nvfp4_scale_bytes(M, K) + 2 * M * N
+        b_pre = N * K // 2 + nv.nvfp4_scale_bytes(N, K) + 2 * M * K + 2 * M * N
+        pre[f"M{M}"] = {"quant_gemm_us": round(tq * 1e6, 2), "quant_gemm": _roof(fl, b_pre, tq, hbm, fp4_peak),
+                        "gemm_us": round(tg * 1e6, 2), "gemm": _roof(fl, b_gemm, tg, hbm, fp4_peak)}
+    out["prefill_fused_qkv_N7168_K5120"] = pre
+    # MoE layers
+    for name, cfg, W, g1, a13, g2, a2 in (
+            ("moe_E128_H2048_I768", synthdata.MOE_SMALL, wl.moe_W, wl.moe_g_a1, wl.moe_a13, wl.moe_g_a2, wl.moe_a2),
+            ("moe_E256_H7168_I2048", synthdata.MOE_LARGE) + wl.large_moe()):
+        E, H, I, topk = cfg["E"], cfg["H"], cfg["I"], cfg["topk"]
+        res = {}
+        ws = torch.empty(nv.nvfp4_moe_workspace(max(cfg["tokens"]), H, I, E, topk), dtype=torch.uint8, device=dev)
+        for T in cfg["tokens"]:
+            c = synthdata.moe_case(T, E, H, I, topk, cfg["skewed"], seed=0, device=dev)
+            o = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+
+            def layer(c=c, o=o):
+                nv.nvfp4_moe_w4a4(c.x, c.topk_ids, c.topk_w, g1, W.w13_codes, W.w13_sf, a13, g2, W.w2_codes,
+                                  W.w2_sf, a2, E, I, out=o, workspace=ws)
+            layer()
+            t = _median_ms(layer, flush, reps, stream) * 1e-3
+            nb, used = _moe_bytes(nv, c.topk_ids, T, E, H, I, topk)
+            res[f"T{T}"] = dict(ms=round(t * 1e3, 4), experts_used=used,
+                                **_roof(2.0 * T * topk * 3 * H * I, nb, t, hbm, fp4_peak))
+            del c, o
+        out[name] = res
+        del ws
+    torch.cuda.synchronize()
+    return out
+
+
 def run_ours(args, world, rank, local):
     import nvfp4_block_scaled_act_gb300 as nv
     from nvfp4_block_scaled_act_gb300 import build
@@ -363,6 +482,8 @@ def run_ours(args, world, rank, local):
             step(recs)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+        hbm, bf16, bf16_sus, peak_src = _peaks()
+        configs = None if args.no_sweep else sweep_configs(wl, nv, dev, hbm, bf16 * FP4_OVER_BF16)
     if world > 1:
         torch.distributed.barrier()
     # device times
@@ -424,8 +545,10 @@ def run_ours(args, world, rank, local):
                 "roofline_bound": "hbm" if wl.moe_bytes / (hbm * 1e9) > wl.moe_flops / (fp4_peak * 1e12) else "tensor",
                 "frac_roofline": round(max(wl.moe_flops / (fp4_peak * 1e12), wl.moe_bytes / (hbm * 1e9)) / t_moe, 4)},
         "moe_w4a16": moe16,
-        # the dominant kernel of the step (about 90 % of its device time, see
-        # profiles/launches_bench_step.md) is the decode GEMM; its roofline is
+        # every workload shape, timed after the step (see sweep_configs)
+        "configs": configs,
+        # the dominant kernel of the step (most of its device time, by the ncu
+        # launch list of this command) is the decode GEMM; its roofline is
         # given for the headline decode call, T = 1 on 8704 x 5120
         "roofline": {"kernel": "gemv_ring_kernel<0> (W4A16 decode, T=1, 8704x5120)", "bound": "hbm",
                      "achieved": round(head["gbs"], 1), "peak": hbm, "unit": "GB/s",
@@ -661,6 +784,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the per-config sweep after the timed steps")
     ap.add_argument("--profile", choices=["gemm", "quant", "gemv", "moe", "moe16"],
                     help="launch one stage a few times on a small case (for ncu), print nothing else")
     ap.add_argument("--reps", type=int, default=3)
