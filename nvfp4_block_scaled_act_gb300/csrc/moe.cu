@@ -4,7 +4,8 @@
 // page, section "Changes").
 //
 // align: a stable counting sort of the T * topk routes by expert, each
-// expert's segment padded to a multiple of 128 rows (one GEMM tile):
+// expert's segment padded to a multiple of 128 rows (one GEMM tile).  Up to
+// 4096 routes one block does it all (moe_align_block_kernel); above that:
 //   moe_hist_kernel     per 1024-route chunk, routes per expert
 //   moe_scan_kernel     one block: expert offsets, padded tile table,
 //                       per-chunk bases, padding rows of row_map
@@ -23,6 +24,7 @@
 namespace nvfp4 {
 
 constexpr int kChunk = 1024;  // routes per histogram / scatter block
+constexpr int kIdBatch = 8;   // global loads a thread keeps in flight in the align kernels
 
 __global__ void __launch_bounds__(256) moe_hist_kernel(const int32_t* __restrict__ ids, int64_t R, int E,
                                                        int32_t* __restrict__ hist, int* status) {
@@ -51,9 +53,17 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ hi
                                                         int32_t* __restrict__ tile_expert) {
   __shared__ int32_t warp_sums[32];
   const int e = threadIdx.x;
+  // the expert's column of the chunk histogram, kIdBatch loads in flight
   int32_t cnt = 0;
-  if (e < E)
-    for (int c = 0; c < nchunks; ++c) cnt += hist[static_cast<int64_t>(c) * E + e];
+  if (e < E) {
+    for (int c0 = 0; c0 < nchunks; c0 += kIdBatch) {
+      int32_t h[kIdBatch];
+#pragma unroll
+      for (int q = 0; q < kIdBatch; ++q) h[q] = c0 + q < nchunks ? hist[static_cast<int64_t>(c0 + q) * E + e] : 0;
+#pragma unroll
+      for (int q = 0; q < kIdBatch; ++q) cnt += h[q];
+    }
+  }
   const int32_t padded = (cnt + 127) / 128 * 128;
   // exclusive scan of padded over experts (block-wide)
   int32_t v = padded;
@@ -82,11 +92,15 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ hi
     offsets[e] = off;
     // per-chunk bases, in chunk order
     int32_t run = off;
-    for (int c = 0; c < nchunks; ++c) {
-      const int64_t idx = static_cast<int64_t>(c) * E + e;
-      const int32_t h = hist[idx];
-      hist[idx] = run;
-      run += h;
+    for (int c0 = 0; c0 < nchunks; c0 += kIdBatch) {
+      int32_t h[kIdBatch];
+#pragma unroll
+      for (int q = 0; q < kIdBatch; ++q) h[q] = c0 + q < nchunks ? hist[static_cast<int64_t>(c0 + q) * E + e] : 0;
+#pragma unroll
+      for (int q = 0; q < kIdBatch; ++q) {
+        if (c0 + q < nchunks) hist[static_cast<int64_t>(c0 + q) * E + e] = run;
+        run += h[q];
+      }
     }
     for (int32_t p = off + cnt; p < off + padded; ++p) row_map[p] = -1;
     for (int32_t p = off; p < off + padded; p += 128) tile_expert[p / 128] = e;
@@ -97,7 +111,10 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ hi
   }
 }
 
-// One warp per chunk; routes in order, 32 at a time.
+// One warp per chunk; routes in order, 32 at a time.  The ids of a chunk are
+// loaded in batches of kIdBatch per lane before they are ranked, so the loads
+// of a batch are in flight together.
+
 __global__ void __launch_bounds__(32) moe_scatter_kernel(const int32_t* __restrict__ ids, int64_t R, int E,
                                                          const int32_t* __restrict__ hist,
                                                          int32_t* __restrict__ row_map, int32_t* __restrict__ pos) {
@@ -106,24 +123,138 @@ __global__ void __launch_bounds__(32) moe_scatter_kernel(const int32_t* __restri
   __syncwarp();
   const int lane = threadIdx.x;
   const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunk;
-  for (int i0 = 0; i0 < kChunk; i0 += 32) {
-    const int64_t r = base + i0 + lane;
-    const bool in = r < R;
-    const int e = in ? ids[r] : -1;
-    const bool valid = in && e >= 0 && e < E;
-    const unsigned key = valid ? static_cast<unsigned>(e) : 0xFFFFFFFFu;
-    const unsigned same = __match_any_sync(0xFFFFFFFFu, key);
-    const int rank = __popc(same & ((1u << lane) - 1u));
-    int32_t p = -1;
-    if (valid) {
-      p = run[e] + rank;
-      row_map[p] = static_cast<int32_t>(r);
+  for (int i0 = 0; i0 < kChunk; i0 += 32 * kIdBatch) {
+    int ev[kIdBatch];
+#pragma unroll
+    for (int q = 0; q < kIdBatch; ++q) {
+      const int64_t r = base + i0 + q * 32 + lane;
+      ev[q] = r < R ? __ldg(ids + r) : -1;
     }
-    if (in) pos[r] = p;
-    __syncwarp();
-    if (valid && rank == 0) run[e] += __popc(same);
-    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < kIdBatch; ++q) {
+      const int64_t r = base + i0 + q * 32 + lane;
+      const bool in = r < R;
+      const int e = ev[q];
+      const bool valid = in && e >= 0 && e < E;
+      const unsigned key = valid ? static_cast<unsigned>(e) : 0xFFFFFFFFu;
+      const unsigned same = __match_any_sync(0xFFFFFFFFu, key);
+      const int rank = __popc(same & ((1u << lane) - 1u));
+      int32_t p = -1;
+      if (valid) {
+        p = run[e] + rank;
+        row_map[p] = static_cast<int32_t>(r);
+      }
+      if (in) pos[r] = p;
+      __syncwarp();
+      if (valid && rank == 0) run[e] += __popc(same);
+      __syncwarp();
+    }
   }
+}
+
+// The whole alignment in one block of 32 warps, for up to kAlignOneBlock
+// routes: warp w counts its contiguous share of the routes per expert into
+// its own shared-memory histogram, one thread per expert scans the padded
+// counts and turns the warp histograms into per-warp bases (in warp order),
+// and each warp places its routes in order.  The layout is the stable counting
+// sort of the multi-block path.
+constexpr int64_t kAlignOneBlock = 4096;  // above this, one SM's rank matching is the bound
+
+__global__ void __launch_bounds__(1024) moe_align_block_kernel(const int32_t* __restrict__ ids, int64_t R, int E,
+                                                               int32_t* __restrict__ counts,
+                                                               int32_t* __restrict__ offsets,
+                                                               int32_t* __restrict__ n_tiles,
+                                                               int32_t* __restrict__ row_map,
+                                                               int32_t* __restrict__ tile_expert,
+                                                               int32_t* __restrict__ pos, int* status) {
+  extern __shared__ int32_t wh[];  // [32][E]
+  __shared__ int32_t warp_sums[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wh[i] = 0;
+  __syncthreads();
+  const int64_t share = (R + 32 * 32 - 1) / (32 * 32) * 32;  // routes per warp, a multiple of 32
+  const int64_t begin = warp * share, end = begin + share < R ? begin + share : R;
+  int32_t* mine = wh + warp * E;
+  bool bad = false;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int64_t i0 = begin; i0 < end; i0 += 32 * kIdBatch) {
+      int ev[kIdBatch];
+#pragma unroll
+      for (int q = 0; q < kIdBatch; ++q) {
+        const int64_t r = i0 + q * 32 + lane;
+        ev[q] = r < end ? __ldg(ids + r) : -1;
+      }
+#pragma unroll
+      for (int q = 0; q < kIdBatch; ++q) {
+        const int64_t r = i0 + q * 32 + lane;
+        if (i0 + q * 32 >= end) break;  // warp-uniform
+        const bool in = r < end;
+        const int e = ev[q];
+        const bool valid = in && e >= 0 && e < E;
+        if (in && !valid) bad = true;
+        const unsigned key = valid ? static_cast<unsigned>(e) : 0xFFFFFFFFu;
+        const unsigned same = __match_any_sync(0xFFFFFFFFu, key);
+        const int rank = __popc(same & ((1u << lane) - 1u));
+        if (pass == 1) {
+          int32_t p = -1;
+          if (valid) {
+            p = mine[e] + rank;
+            row_map[p] = static_cast<int32_t>(r);
+          }
+          if (in) pos[r] = p;
+        }
+        __syncwarp();
+        if (valid && rank == 0) mine[e] += __popc(same);
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+    if (pass == 1) break;
+    // one thread per expert (E <= 1024): counts, padded offsets, per-warp bases
+    const int e = threadIdx.x;
+    int32_t cnt = 0;
+    if (e < E)
+      for (int w = 0; w < 32; ++w) cnt += wh[w * E + e];
+    const int32_t padded = (cnt + 127) / 128 * 128;
+    int32_t v = padded;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+      if (lane >= o) v += t;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int32_t s2 = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t t = __shfl_up_sync(0xFFFFFFFFu, s2, o);
+        if (lane >= o) s2 += t;
+      }
+      warp_sums[lane] = s2;
+    }
+    __syncthreads();
+    const int32_t incl = v + (warp > 0 ? warp_sums[warp - 1] : 0);
+    const int32_t off = incl - padded;
+    if (e < E) {
+      counts[e] = cnt;
+      offsets[e] = off;
+      int32_t run = off;
+      for (int w = 0; w < 32; ++w) {
+        const int32_t h = wh[w * E + e];
+        wh[w * E + e] = run;
+        run += h;
+      }
+      for (int32_t p = off + cnt; p < off + padded; ++p) row_map[p] = -1;
+      for (int32_t p = off; p < off + padded; p += 128) tile_expert[p / 128] = e;
+    }
+    if (e == E - 1) {
+      offsets[E] = incl;
+      *n_tiles = incl / 128;
+    }
+    __syncthreads();
+  }
+  if (bad) record_status(status, kStatusBadExpert);
 }
 
 // x [T, H] bf16 -> NVFP4 rows of a1 at pos[t * topk + s]; clears y [T, H].
@@ -234,6 +365,17 @@ __global__ void __launch_bounds__(1024) moe_calib_finish_kernel(unsigned int* __
 cudaError_t launch_moe_align(const int32_t* ids, int64_t T, int topk, int E, const MoEWorkspace& w, int* status,
                              cudaStream_t stream) {
   const int64_t R = T * topk;
+  if (R <= kAlignOneBlock && E <= 1024) {
+    const size_t smem = 32 * static_cast<size_t>(E) * sizeof(int32_t);
+    if (smem > 48 * 1024) {  // per device: set on every launch
+      const cudaError_t e = cudaFuncSetAttribute(moe_align_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+    }
+    moe_align_block_kernel<<<1, 1024, smem, stream>>>(
+        ids, R, E, w.counts, w.offsets, w.n_tiles, w.row_map, w.tile_expert, w.pos, status);
+    return cudaGetLastError();
+  }
   const int nchunks = static_cast<int>((R + kChunk - 1) / kChunk);
   moe_hist_kernel<<<nchunks, 256, E * sizeof(int32_t), stream>>>(ids, R, E, w.hist, status);
   moe_scan_kernel<<<1, 1024, 0, stream>>>(w.hist, nchunks, E, w.counts, w.offsets, w.n_tiles, w.row_map,
