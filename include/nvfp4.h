@@ -98,7 +98,8 @@ nvfp4_status nvfp4_reduce_max(const float* d_in, int64_t n, float* d_out, nvfp4_
  * all codes +0 when s == 0.
  *   x_bf16  [M, K] bf16, row stride ldx >= K elements, ldx % 8 == 0
  *   K       multiple of 16
- *   d_global one fp32 (g)
+ *   d_global one fp32 (g), 0 < g <= 6.6e35 so that g / s stays finite for
+ *           every E4M3 scale s (the smallest is 2^-9)
  *   codes   [M, K/2] bytes, written
  *   scales  nvfp4_scale_bytes(M, K) bytes, written in full (padding zeroed)
  * Codes and scales are bit-identical to the reference rule for any finite input. */

@@ -105,6 +105,10 @@ float nvo_e4m3_to_f32(uint8_t b) {
 uint8_t nvo_f32_to_e4m3_satfinite(float f) {
   double a = fabs((double)f);
   uint8_t sign = signbit(f) ? 0x80 : 0x00;
+  /* satfinite: a magnitude at or beyond the largest finite value (448) maps to
+   * it; said explicitly because the distances below stop telling candidates
+   * apart once a is huge (or infinite) */
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);
   int best = 0;
   double bestd = INFINITY;
   for (int c = 0; c <= 0x7E; ++c) {
@@ -135,6 +139,10 @@ float nvo_e2m1_to_f32(uint8_t code) {
 uint8_t nvo_f32_to_e2m1_satfinite(float f) {
   double a = fabs((double)f);
   uint8_t sign = signbit(f) ? 0x8 : 0x0;
+  /* satfinite: a magnitude at or beyond the largest finite value (6) maps to
+   * it; said explicitly because the distances below stop telling candidates
+   * apart once a is huge (or infinite) */
+  if (a >= 6.0) return (uint8_t)(sign | 7);
   int best = 0;
   double bestd = INFINITY;
   for (int c = 0; c < 8; ++c) {

@@ -112,6 +112,22 @@ def test_e4m3_ties(lib):
     assert_same_quant(lib, x, 1.0)
 
 
+@pytest.mark.parametrize("g", [1.0, 2688.0 / 3.0, 1e-3, 7.7e4, 1.0e30])
+def test_every_bf16_block_maximum(lib, g):
+    """One block per non-negative finite bf16 value v (subnormals included) with
+    v as its largest magnitude: the scale step amax / 6 is exact against the
+    oracle's IEEE division for every input the quantiser can see.  With the
+    large globals, x * r overflows fp32 for the largest blocks and satfinite
+    clamps the codes to 6 on both sides."""
+    bits = torch.arange(0, 0x7F80, dtype=torch.int32).to(torch.int16)
+    v = bits.view(torch.bfloat16).float()
+    frac = torch.tensor([1.0, -0.9, 0.75, -0.6, 0.5, -0.41, 0.33, -0.25, 0.2, -0.17, 0.12, -0.08, 0.05, -0.03,
+                         0.01, -1.0])
+    rows = (v[:, None] * frac[None, :]).to(torch.bfloat16)
+    rows[:, 0] = v.to(torch.bfloat16)
+    assert_same_quant(lib, rows, g)
+
+
 def test_random_exponent_sweep(lib):
     rng = np.random.default_rng(11)
     M, K = 256, 256

@@ -145,6 +145,17 @@ def test_e2m1_ties_to_even_and_saturation(y, code):
     assert oracle.f32_to_e2m1(y) == code
 
 
+def test_satfinite_conversions_clamp_an_overflowed_product():
+    """A product x * r far above the format's range (an activation far above the
+    calibration amax, or an fp32 overflow to +-inf) is clamped by satfinite to
+    the largest finite value: 6 for e2m1, 448 for E4M3."""
+    inf = float("inf")
+    for v in (6.0, 6.5, 7.0, 1.0e17, 3.0e38, inf):
+        assert oracle.f32_to_e2m1(v) == 0x7 and oracle.f32_to_e2m1(-v) == 0xF, v
+    for v in (448.0, 460.0, 470.0, 1.0e20, 3.0e38, inf):
+        assert oracle.f32_to_e4m3(v) == 0x7E and oracle.f32_to_e4m3(-v) == 0xFE, v
+
+
 def test_e2m1_nearest_brute_force():
     grid = e2m1_grid_from_definition()[:8]
     rng = np.random.default_rng(3)
