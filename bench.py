@@ -416,6 +416,31 @@ def sweep_configs(wl, nv, dev, hbm, fp4_peak, reps=5):
         pre[f"M{M}"] = {"quant_gemm_us": round(tq * 1e6, 2), "quant_gemm": _roof(fl, b_pre, tq, hbm, fp4_peak),
                         "gemm_us": round(tg * 1e6, 2), "gemm": _roof(fl, b_gemm, tg, hbm, fp4_peak)}
     out["prefill_fused_qkv_N7168_K5120"] = pre
+    # a stack of 8 prefill layers (quantise + GEMM, M = 8192) on 8 distinct
+    # weight copies in one CUDA graph: the activations of a layer and its
+    # output meet the next layer's weights in L2
+    M = synthdata.PREFILL_M[-1]
+    copies = [(wl.pre_W.codes, wl.pre_W.scales)] + [(wl.pre_W.codes.clone(), wl.pre_W.scales.clone())
+                                                    for _ in range(7)]
+
+    def stack():
+        for c, sc in copies:
+            nv.nvfp4_quantize_act(wl.pre_x, wl.pre_g, wl.pre_codes, wl.pre_sf)
+            nv.nvfp4_linear_w4a4(wl.pre_codes, wl.pre_sf, c, sc, wl.pre_alpha, N, K, out=wl.pre_out)
+    s2 = torch.cuda.Stream()
+    s2.wait_stream(stream)
+    with torch.cuda.stream(s2):
+        stack()
+    stream.wait_stream(s2)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        stack()
+    t = _median_ms(g.replay, flush, reps, stream) * 1e-3 / len(copies)
+    fl = 2.0 * M * N * K
+    b_pre = N * K // 2 + nv.nvfp4_scale_bytes(N, K) + 2 * M * K + 2 * M * N
+    out["prefill_stack_8_layers_M8192"] = dict(us_per_layer=round(t * 1e6, 2), **_roof(fl, b_pre, t, hbm, fp4_peak))
+    del copies, g
     # MoE layers
     for name, cfg, W, g1, a13, g2, a2 in (
             ("moe_E128_H2048_I768", synthdata.MOE_SMALL, wl.moe_W, wl.moe_g_a1, wl.moe_a13, wl.moe_g_a2, wl.moe_a2),

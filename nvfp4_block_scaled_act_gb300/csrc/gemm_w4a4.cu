@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   if (b_row[j] < p.b_rows_total) bytes += 128 * 128;
               }
               mbar_arrive_expect_tx(&full_bar[stage], bytes);
-              if (mvalid) tma_load_2d(sA, &tmA, &full_bar[stage], kb * 128, mt * 128);
+              if (mvalid) tma_load_2d_hint(sA, &tmA, &full_bar[stage], kb * 128, mt * 128, act_policy());
               if (MODE == kEpiDense) {
                 if (b_row[0] < p.b_rows_total) tma_load_2d(sB, &tmB, &full_bar[stage], kb * 128, b_row[0]);
               } else {
@@ -702,7 +702,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!scale_role) {
               const bool bvalid = b_row < p.b_rows_total;
               mbar_arrive_expect_tx(&full_bar[stage], (mvalid ? Cfg::A_BYTES : 0) + (bvalid ? Cfg::B_BYTES : 0));
-              if (mvalid) tma_load_2d(sA, &tmA, &full_bar[stage], kb * 128, mt * 128);
+              if (mvalid) tma_load_2d_hint(sA, &tmA, &full_bar[stage], kb * 128, mt * 128, act_policy());
               if (bvalid) tma_load_2d(sB, &tmB, &full_bar[stage], kb * 128, b_row);
             } else {
               uint32_t bytes = mvalid ? ks * 512 : 0;

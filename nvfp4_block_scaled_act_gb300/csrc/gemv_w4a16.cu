@@ -409,8 +409,7 @@ __global__ void __launch_bounds__(RingShape<kTok16>::kThreads, RingShape<kTok16>
           v[q] = make_uint4(0u, 0u, 0u, 0u);
           if (p < npairs) {
             const int tok = p / nkb, kb = p - (p / nkb) * nkb;
-            v[q] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * ldx + k_begin + kb * 128 +
-                                                        l16 * 8));
+            v[q] = ldg_v4_hint(x + static_cast<int64_t>(tok) * ldx + k_begin + kb * 128 + l16 * 8, act_policy());
           }
         }
 #pragma unroll
@@ -586,7 +585,9 @@ __global__ void __launch_bounds__(RingShape<kTok16>::kThreads, RingShape<kTok16>
       float sum = 0.0f;
       for (int q = 0; q < static_cast<int>(ncl); ++q) sum += recv[(q * T + tok) * rows_per + rl];
       const int n = rb * kRingRows + static_cast<int>(rank) * rows_per + rl;
-      if (n < N) out[static_cast<int64_t>(tok) * ldo + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum * alpha));
+      if (n < N)
+        stg_u16_hint(out + static_cast<int64_t>(tok) * ldo + n, __bfloat16_as_ushort(__float2bfloat16_rn(sum * alpha)),
+                     act_policy());  // the next layer's input
     }
   }
 }

@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restri
   }
   __syncthreads();
   const int lane = threadIdx.x & 31;
+  const uint64_t pol = act_policy();  // the codes are read next by the GEMM
   const uint32_t chunks = static_cast<uint32_t>((Cp + 31) / 32);       // 512-element chunks per row
   const uint32_t groups = (chunks + kQuantUnroll - 1) / kQuantUnroll;  // items per row
   const uint32_t total = static_cast<uint32_t>(Mp) * groups;
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restri
             packed[h] = f32x8_to_e2m1x8(v, rr);
           }
         }
-        *reinterpret_cast<uint2*>(crow + static_cast<int64_t>(cc) * 8) = make_uint2(packed[0], packed[1]);
+        stg_v2_hint(crow + static_cast<int64_t>(cc) * 8, packed[0], packed[1], pol);
       }
       if (cc < Cp) srow[(cc >> 2) * 512 + (cc & 3)] = real ? static_cast<uint8_t>(s8) : 0;
     }
