@@ -416,6 +416,45 @@ def sweep_configs(wl, nv, dev, hbm, fp4_peak, reps=5):
         pre[f"M{M}"] = {"quant_gemm_us": round(tq * 1e6, 2), "quant_gemm": _roof(fl, b_pre, tq, hbm, fp4_peak),
                         "gemm_us": round(tg * 1e6, 2), "gemm": _roof(fl, b_gemm, tg, hbm, fp4_peak)}
     out["prefill_fused_qkv_N7168_K5120"] = pre
+    # small batches on the fused qkv weight: the W4A4 GEMM beside the W4A16
+    # decode GEMM, each a CUDA graph over 16 weight copies (cold weights)
+    small = {}
+    copies16 = [(wl.pre_W.codes, wl.pre_W.scales)] + [(wl.pre_W.codes.clone(), wl.pre_W.scales.clone())
+                                                      for _ in range(15)]
+    alpha16 = nv.nvfp4_make_alpha(None, wl.pre_W.g)
+    wbytes = N * K // 2 + nv.nvfp4_scale_bytes(N, K)
+
+    def graph_us(call):
+        s2 = torch.cuda.Stream()
+        s2.wait_stream(stream)
+        with torch.cuda.stream(s2):
+            call(0)
+        stream.wait_stream(s2)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for j in range(len(copies16)):
+                call(j)
+        return _median_ms(g.replay, flush, reps, stream) * 1e3 / len(copies16)
+
+    for M in (1, 8, 16, 32, 48, 64, 128, 256):
+        x = wl.pre_x[:M]
+        codes, sf = nv.nvfp4_quantize_act(x, wl.pre_g)
+        o = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+
+        def w4a4(j, codes=codes, sf=sf, o=o):
+            nv.nvfp4_linear_w4a4(codes, sf, copies16[j][0], copies16[j][1], wl.pre_alpha, N, K, out=o)
+        entry = {"w4a4_gemm_us": round(graph_us(w4a4), 2)}
+        entry["w4a4_gbs"] = round(wbytes / entry["w4a4_gemm_us"] / 1e3, 1)
+        if M <= 16:
+            ws = torch.empty(max(nv.nvfp4_linear_w4a16_workspace(M, N, K), 16), dtype=torch.uint8, device=dev)
+
+            def w4a16(j, x=x, o=o, ws=ws):
+                nv.nvfp4_linear_w4a16(x, copies16[j][0], copies16[j][1], alpha16, N, K, out=o, workspace=ws)
+            entry["w4a16_us"] = round(graph_us(w4a16), 2)
+        small[f"M{M}"] = entry
+    out["small_batch_fused_qkv_N7168_K5120"] = small
+    del copies16
     # a stack of 8 prefill layers (quantise + GEMM, M = 8192) on 8 distinct
     # weight copies in one CUDA graph: the activations of a layer and its
     # output meet the next layer's weights in L2

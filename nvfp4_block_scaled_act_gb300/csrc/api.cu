@@ -273,6 +273,9 @@ nvfp4_status nvfp4_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx
   return cuda_status(launch_quant_act(x, M, K, ldx, d_global, codes, scales, dev->sms, stream));
 }
 
+// Up to this many rows the dense W4A4 linear runs on 128 x 128 tiles.
+constexpr int64_t kSmallM = 128;
+
 nvfp4_status nvfp4_linear_w4a4(const uint8_t* a_codes, const uint8_t* a_sf, int64_t M, const uint8_t* w_codes,
                                const uint8_t* w_sf, int64_t N, int64_t K, const float* d_alpha, void* out,
                                int64_t ldo, nvfp4_stream_t stream) {
@@ -306,6 +309,13 @@ nvfp4_status nvfp4_linear_w4a4(const uint8_t* a_codes, const uint8_t* a_sf, int6
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.status = dev->status;
+  if (M <= kSmallM) {
+    // few tokens: 128 x 128 tiles on single CTAs, one per SM at most
+    p.n_tiles = static_cast<int>((N + 127) / 128);
+    const int64_t tiles = m_tiles * p.n_tiles;
+    const int64_t grid = tiles < dev->sms ? tiles : dev->sms;
+    return cuda_status(launch_gemm(kLaunchDenseSmall, maps, p, static_cast<int>(grid), stream));
+  }
   // one CTA pair per 256 x 256 tile, at most one pair per two SMs
   const int64_t units = ((m_tiles + 1) / 2) * p.n_tiles;
   const int64_t pairs = units < dev->sms / 2 ? units : dev->sms / 2;

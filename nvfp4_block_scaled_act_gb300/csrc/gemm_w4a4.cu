@@ -931,6 +931,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 using GatedCfg = GemmCfg<256, 1, 4, kEpiGatedQuant>;
 using AmaxCfg = GemmCfg<256, 1, 4, kEpiGatedAmax>;
 using DownCfg = GemmCfg<128, 2, 4, kEpiDownSum>;
+using DenseSmallCfg = GemmCfg<128, 2, 6, kEpiDense>;  // 6 x 36 KB stages, 2 x 128 + 6 x 32 TMEM columns
 
 template <class Cfg>
 static cudaError_t launch_cfg(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {
@@ -965,6 +966,7 @@ cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int
     case kEpiGatedQuant: return launch_cfg<GatedCfg>(maps, p, grid, stream);
     case kEpiGatedAmax: return launch_cfg<AmaxCfg>(maps, p, grid, stream);
     case kEpiDownSum: return launch_cfg<DownCfg>(maps, p, grid, stream);
+    case kLaunchDenseSmall: return launch_cfg<DenseSmallCfg>(maps, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -19,6 +19,10 @@ cudaError_t launch_reduce_max(const float* d_in, int64_t n, float* d_out, cudaSt
 
 // ---- block-scaled tcgen05 GEMM (gemm_w4a4.cu) ------------------------------
 enum EpiMode : int { kEpiDense = 0, kEpiGatedQuant = 1, kEpiGatedAmax = 2, kEpiDownSum = 3 };
+// Launch mode of the dense W4A4 linear for small M: the single-CTA kernel on
+// 128 x 128 tiles (twice the CTAs of the pair kernel's 256 x 256 tiles, a
+// deeper stage ring), dense epilogue.
+constexpr int kLaunchDenseSmall = 4;
 
 struct GemmParams {
   const uint8_t* sfa;      // swizzled scales of A (over all A rows)

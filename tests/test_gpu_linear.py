@@ -79,6 +79,18 @@ def test_w4a4_ragged_shapes(nv, M, N, K):
     check_close(L.w4a4(nv), L.w4a4_oracle(), f"W4A4 {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M", [1, 8, 17, 48, 100, 128, 129, 256])
+def test_w4a4_small_m_fused_qkv(nv, M):
+    """Small batches on the fused qkv weight (N = 7168, K = 5120): up to 128 rows
+    run on 128 x 128 single-CTA tiles, above that on CTA pairs; every row is
+    compared with the oracle, and a repeated call gives the same bits."""
+    L = Linear(nv, synthdata.prefill_case(M, seed=M))
+    out = L.w4a4(nv)
+    check_close(out, L.w4a4_oracle(), f"small-M W4A4 M={M}")
+    assert torch.equal(L.w4a4(nv), out), f"small-M W4A4 M={M} is not repeatable"
+    assert nv.nvfp4_device_status() == 0
+
+
 def test_w4a4_row_strided_output_and_repeatability(nv):
     L = Linear(nv, synthdata.linear_case(200, 256, 512, seed=3))
     big = torch.full((200, 264), float("nan"), dtype=torch.bfloat16, device=DEV)
