@@ -122,7 +122,8 @@ MoELayoutBytes moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t to
   MoELayoutBytes L{};
   const int64_t R = T * topk;
   const int64_t p_max = (R + E * 127 + 127) / 128 * 128;
-  const int64_t nchunks = (R + 1023) / 1024;
+  const int64_t chunk = nvfp4::moe_align_chunk(R);
+  const int64_t nchunks = (R + chunk - 1) / chunk;
   L.p_max = p_max;
   size_t off = 0;
   auto take = [&](size_t bytes) {

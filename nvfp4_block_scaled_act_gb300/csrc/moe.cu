@@ -6,10 +6,11 @@
 // align: a stable counting sort of the T * topk routes by expert, each
 // expert's segment padded to a multiple of 128 rows (one GEMM tile).  Up to
 // 4096 routes one block does it all (moe_align_block_kernel); above that:
-//   moe_hist_kernel     per 1024-route chunk, routes per expert
+//   moe_hist_kernel     per chunk of routes (256, doubled while there are
+//                       over 512 chunks), routes per expert
 //   moe_scan_kernel     one block: expert offsets, padded tile table,
 //                       per-chunk bases, padding rows of row_map
-//   moe_scatter_kernel  per chunk, in route order: row_map / pos entries
+//   moe_scatter_kernel  one warp per chunk, in route order: row_map / pos
 // The order inside a segment is the route order, so the layout is the same on
 // every run.  Nothing leaves the device: the tile count is read by the GEMMs.
 //
@@ -23,16 +24,16 @@
 
 namespace nvfp4 {
 
-constexpr int kChunk = 1024;  // routes per histogram / scatter block
-constexpr int kIdBatch = 8;   // global loads a thread keeps in flight in the align kernels
+constexpr int kIdBatch = 8;  // global loads a thread keeps in flight in the align kernels
 
-__global__ void __launch_bounds__(256) moe_hist_kernel(const int32_t* __restrict__ ids, int64_t R, int E,
+// Per chunk of `chunk` routes: routes per expert.
+__global__ void __launch_bounds__(256) moe_hist_kernel(const int32_t* __restrict__ ids, int64_t R, int E, int chunk,
                                                        int32_t* __restrict__ hist, int* status) {
   extern __shared__ int32_t sh[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
   __syncthreads();
-  const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunk;
-  for (int i = threadIdx.x; i < kChunk; i += blockDim.x) {
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * chunk;
+  for (int i = threadIdx.x; i < chunk; i += blockDim.x) {
     const int64_t r = base + i;
     if (r < R) {
       const int e = ids[r];
@@ -46,32 +47,50 @@ __global__ void __launch_bounds__(256) moe_hist_kernel(const int32_t* __restrict
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<int64_t>(blockIdx.x) * E + e] = sh[e];
 }
 
-// One block of up to 1024 threads, one expert per thread.
+// One block of 1024 threads.  Each expert's column of the chunk histogram is
+// split into P = 1024 / E contiguous runs of chunks, one thread per run
+// (thread t: expert t % E, run t / E, so a warp reads consecutive experts of
+// one chunk).  The run sums give the expert counts; one thread per expert scans
+// the padded counts; each run thread then rewrites its chunks as the expert's
+// base for that chunk (in chunk order) and writes its share of the padding
+// rows and tile entries.
 __global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                         int32_t* __restrict__ n_tiles, int32_t* __restrict__ row_map,
                                                         int32_t* __restrict__ tile_expert) {
+  __shared__ int32_t part_s[1024];  // [run][expert] chunk sums
+  __shared__ int32_t off_s[1024];   // [expert] padded segment start
+  __shared__ int32_t cnt_s[1024];   // [expert] routes
   __shared__ int32_t warp_sums[32];
-  const int e = threadIdx.x;
-  // the expert's column of the chunk histogram, kIdBatch loads in flight
-  int32_t cnt = 0;
-  if (e < E) {
-    for (int c0 = 0; c0 < nchunks; c0 += kIdBatch) {
+  const int t = threadIdx.x;
+  const int P = static_cast<int>(blockDim.x) / E;
+  const int e = t % E, run = t / E;
+  const bool active = run < P;
+  const int per = (nchunks + P - 1) / P;
+  const int c_begin = min(run * per, nchunks), c_end = min(c_begin + per, nchunks);
+  int32_t part = 0;
+  if (active) {
+    for (int c0 = c_begin; c0 < c_end; c0 += kIdBatch) {
       int32_t h[kIdBatch];
 #pragma unroll
-      for (int q = 0; q < kIdBatch; ++q) h[q] = c0 + q < nchunks ? hist[static_cast<int64_t>(c0 + q) * E + e] : 0;
+      for (int q = 0; q < kIdBatch; ++q) h[q] = c0 + q < c_end ? hist[static_cast<int64_t>(c0 + q) * E + e] : 0;
 #pragma unroll
-      for (int q = 0; q < kIdBatch; ++q) cnt += h[q];
+      for (int q = 0; q < kIdBatch; ++q) part += h[q];
     }
   }
+  part_s[t] = part;
+  __syncthreads();
+  int32_t cnt = 0;
+  if (t < E)
+    for (int q = 0; q < P; ++q) cnt += part_s[q * E + t];
   const int32_t padded = (cnt + 127) / 128 * 128;
   // exclusive scan of padded over experts (block-wide)
   int32_t v = padded;
-  const int lane = e & 31, w = e >> 5;
+  const int lane = t & 31, w = t >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int32_t t = __shfl_up_sync(0xFFFFFFFFu, v, o);
-    if (lane >= o) v += t;
+    const int32_t s = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += s;
   }
   if (lane == 31) warp_sums[w] = v;
   __syncthreads();
@@ -79,51 +98,56 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ hi
     int32_t s = (lane < static_cast<int>(blockDim.x >> 5)) ? warp_sums[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int32_t t = __shfl_up_sync(0xFFFFFFFFu, s, o);
-      if (lane >= o) s += t;
+      const int32_t u = __shfl_up_sync(0xFFFFFFFFu, s, o);
+      if (lane >= o) s += u;
     }
     warp_sums[lane] = s;
   }
   __syncthreads();
   const int32_t incl = v + (w > 0 ? warp_sums[w - 1] : 0);
-  const int32_t off = incl - padded;
-  if (e < E) {
-    counts[e] = cnt;
-    offsets[e] = off;
-    // per-chunk bases, in chunk order
-    int32_t run = off;
-    for (int c0 = 0; c0 < nchunks; c0 += kIdBatch) {
-      int32_t h[kIdBatch];
-#pragma unroll
-      for (int q = 0; q < kIdBatch; ++q) h[q] = c0 + q < nchunks ? hist[static_cast<int64_t>(c0 + q) * E + e] : 0;
-#pragma unroll
-      for (int q = 0; q < kIdBatch; ++q) {
-        if (c0 + q < nchunks) hist[static_cast<int64_t>(c0 + q) * E + e] = run;
-        run += h[q];
-      }
-    }
-    for (int32_t p = off + cnt; p < off + padded; ++p) row_map[p] = -1;
-    for (int32_t p = off; p < off + padded; p += 128) tile_expert[p / 128] = e;
+  if (t < E) {
+    const int32_t off = incl - padded;
+    counts[t] = cnt;
+    offsets[t] = off;
+    off_s[t] = off;
+    cnt_s[t] = cnt;
   }
-  if (e == E - 1) {
+  if (t == E - 1) {
     offsets[E] = incl;
     *n_tiles = incl / 128;
+  }
+  __syncthreads();
+  if (active) {
+    const int32_t off = off_s[e], ce = cnt_s[e], pe = (ce + 127) / 128 * 128;
+    int32_t base = off;
+    for (int q = 0; q < run; ++q) base += part_s[q * E + e];
+    for (int c0 = c_begin; c0 < c_end; c0 += kIdBatch) {
+      int32_t h[kIdBatch];
+#pragma unroll
+      for (int q = 0; q < kIdBatch; ++q) h[q] = c0 + q < c_end ? hist[static_cast<int64_t>(c0 + q) * E + e] : 0;
+#pragma unroll
+      for (int q = 0; q < kIdBatch; ++q) {
+        if (c0 + q < c_end) hist[static_cast<int64_t>(c0 + q) * E + e] = base;
+        base += h[q];
+      }
+    }
+    for (int32_t p = off + ce + run; p < off + pe; p += P) row_map[p] = -1;
+    for (int32_t p = off / 128 + run; p < (off + pe) / 128; p += P) tile_expert[p] = e;
   }
 }
 
 // One warp per chunk; routes in order, 32 at a time.  The ids of a chunk are
 // loaded in batches of kIdBatch per lane before they are ranked, so the loads
 // of a batch are in flight together.
-
-__global__ void __launch_bounds__(32) moe_scatter_kernel(const int32_t* __restrict__ ids, int64_t R, int E,
+__global__ void __launch_bounds__(32) moe_scatter_kernel(const int32_t* __restrict__ ids, int64_t R, int E, int chunk,
                                                          const int32_t* __restrict__ hist,
                                                          int32_t* __restrict__ row_map, int32_t* __restrict__ pos) {
   extern __shared__ int32_t run[];
   for (int e = threadIdx.x; e < E; e += 32) run[e] = hist[static_cast<int64_t>(blockIdx.x) * E + e];
   __syncwarp();
   const int lane = threadIdx.x;
-  const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunk;
-  for (int i0 = 0; i0 < kChunk; i0 += 32 * kIdBatch) {
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * chunk;
+  for (int i0 = 0; i0 < chunk; i0 += 32 * kIdBatch) {
     int ev[kIdBatch];
 #pragma unroll
     for (int q = 0; q < kIdBatch; ++q) {
@@ -376,11 +400,14 @@ cudaError_t launch_moe_align(const int32_t* ids, int64_t T, int topk, int E, con
         ids, R, E, w.counts, w.offsets, w.n_tiles, w.row_map, w.tile_expert, w.pos, status);
     return cudaGetLastError();
   }
-  const int nchunks = static_cast<int>((R + kChunk - 1) / kChunk);
-  moe_hist_kernel<<<nchunks, 256, E * sizeof(int32_t), stream>>>(ids, R, E, w.hist, status);
+  const int64_t chunk = moe_align_chunk(R);
+  const int nchunks = static_cast<int>((R + chunk - 1) / chunk);
+  moe_hist_kernel<<<nchunks, 256, E * sizeof(int32_t), stream>>>(ids, R, E, static_cast<int>(chunk), w.hist,
+                                                                  status);
   moe_scan_kernel<<<1, 1024, 0, stream>>>(w.hist, nchunks, E, w.counts, w.offsets, w.n_tiles, w.row_map,
                                           w.tile_expert);
-  moe_scatter_kernel<<<nchunks, 32, E * sizeof(int32_t), stream>>>(ids, R, E, w.hist, w.row_map, w.pos);
+  moe_scatter_kernel<<<nchunks, 32, E * sizeof(int32_t), stream>>>(ids, R, E, static_cast<int>(chunk), w.hist,
+                                                                   w.row_map, w.pos);
   return cudaGetLastError();
 }
 

@@ -32,6 +32,16 @@ struct MoELayoutBytes {
   int64_t p_max;
 };
 
+// Routes per histogram / scatter chunk of the multi-block align: 256, doubled
+// until there are at most 512 chunks, so the scatter has a warp per 256-512
+// routes and the scan's per-expert column stays short.  The workspace sizes the
+// chunk histogram with the same rule.
+inline int64_t moe_align_chunk(int64_t R) {
+  int64_t c = 256;
+  while ((R + c - 1) / c > 512) c *= 2;
+  return c;
+}
+
 MoELayoutBytes moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk);
 MoEWorkspace moe_carve(void* base, const MoELayoutBytes& L);
 
