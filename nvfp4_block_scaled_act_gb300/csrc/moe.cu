@@ -16,7 +16,8 @@
 //
 // quant_permute: the NVFP4 quantisation of x with the static global g_a1, one
 // warp per 256-element chunk of a token row, written to each of the token's
-// permuted rows; it also clears the fp32 top-k accumulator y.
+// permuted rows (codes as one 128-byte row segment per warp, scales as 4-byte
+// words of four blocks); it also clears the fp32 top-k accumulator y.
 // finalize: y (fp32) -> bf16.
 #include "nvfp4_common.cuh"
 #include "nvfp4_internal.h"
@@ -327,12 +328,26 @@ __global__ void __launch_bounds__(256) moe_quant_permute_kernel(const uint16_t* 
         packed |= f32x2_to_e2m1x2(__fmul_rn(v[2 * j], bs.r), __fmul_rn(v[2 * j + 1], bs.r)) << (8 * j);
     }
     if (real) {
-      const int64_t c = k0 / 16;
       for (int s = 0; s < topk; ++s) {
         const int32_t p = pos[t * topk + s];
-        if (p < 0) continue;
-        *reinterpret_cast<uint32_t*>(a_codes + static_cast<int64_t>(p) * (H / 2) + k0 / 2) = packed;
-        if ((lane & 1) == 0) a_sf[sf_offset(p, c, cpad4)] = static_cast<uint8_t>(bs.s8);
+        if (p >= 0) *reinterpret_cast<uint32_t*>(a_codes + static_cast<int64_t>(p) * (H / 2) + k0 / 2) = packed;
+      }
+    }
+    // scale bytes: block j of the chunk sits on lanes 2j and 2j + 1.  Four
+    // consecutive blocks are four consecutive bytes of the 128x4 layout, so
+    // lane 8w packs blocks 4w .. 4w+3 into a word, and lane l stores word
+    // l % 4 for routes l / 4, l / 4 + 8, ...
+    const uint32_t sv = static_cast<uint32_t>(bs.s8) & 0xFFu;
+    const uint32_t packed_sf = sv | (__shfl_down_sync(0xFFFFFFFFu, sv, 2) << 8) |
+                               (__shfl_down_sync(0xFFFFFFFFu, sv, 4) << 16) |
+                               (__shfl_down_sync(0xFFFFFFFFu, sv, 6) << 24);
+    const int wq = lane & 3;
+    const uint32_t word = __shfl_sync(0xFFFFFFFFu, packed_sf, 8 * wq);
+    const int64_t c = ch * 16 + 4 * wq;
+    if (c * 16 < H) {
+      for (int s = lane >> 2; s < topk; s += 8) {
+        const int32_t p = pos[t * topk + s];
+        if (p >= 0) *reinterpret_cast<uint32_t*>(a_sf + sf_offset(p, c, cpad4)) = word;
       }
     }
   }
