@@ -61,10 +61,10 @@ struct GemmCfg {
   static constexpr int SFA_BYTES = 2048;   // 4 atoms = 256 k of 128 rows
   static constexpr int SFB_BYTES = NBLK * 2048;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  // MoE down: fp32 staging of each epilogue warp's 32 rows x BN/2 columns (row
-  // pitch padded by 16 bytes) for the bulk reduce-add into y
-  static constexpr int EPI_PITCH = (BN / 2) * 4 + 16;
-  static constexpr int EPI_BYTES = MODE_ == 3 ? 8 * 32 * EPI_PITCH : 0;
+  // MoE down: fp32 staging of the 128 rows x BN columns of a tile (row pitch
+  // padded by 16 bytes) for the bulk reduce-adds into y
+  static constexpr int EPI_PITCH = BN * 4 + 16;
+  static constexpr int EPI_BYTES = MODE_ == 3 ? 128 * EPI_PITCH : 0;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024;
   static constexpr int SF_COLS = 16 + 4 * (BN / 32);  // TMEM scale columns per stage
   static constexpr int SF_BASE = NUM_ACC * BN;
@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t accf_bar[NUM_ACC];
   __shared__ __align__(8) uint64_t acce_bar[NUM_ACC];
   __shared__ __align__(8) uint64_t done_bar;
+  __shared__ __align__(8) uint64_t quad_bar[4];  // MoE down: the two epilogue warps of a lane quadrant
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ float r_of_s8[MODE == kEpiGatedQuant ? 256 : 1];  // g_out / S for every E4M3 scale byte
@@ -212,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acce_bar[a], kNumEpi);
     }
     mbar_init(&done_bar, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&quad_bar[i], 2);
     abort_flag = 0;
     fence_barrier_init();
   }
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 8;
     const int q = warp & 3;      // TMEM lane quadrant of this warp
     const int part = ew >> 2;    // column half of this warp within its quadrant
-    uint32_t acc = 0, acc_phase = 0;
+    uint32_t acc = 0, acc_phase = 0, quad_phase = 0;
     const float alpha_dense = (MODE == kEpiDense) ? __ldg(p.alpha) : 0.0f;
     const float g_out = (MODE == kEpiGatedQuant) ? __ldg(p.g_out) : 0.0f;
     for (int tile = unit0; tile < total; tile += unit_step) {
@@ -495,12 +497,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < COLS / 32; ++c) store_bf16_32(dst + 32 * c, r[c], alpha_dense, p.N - nbase - 32 * c);
           }
         } else {
-          // w * alpha_e * acc of this row -> the warp's staging row -> one bulk
-          // reduce-add (fp32) into the token's row of y
-          float* stg = reinterpret_cast<float*>(smem + STAGES * Cfg::STAGE_BYTES + (ew * 32 + lane) * Cfg::EPI_PITCH);
-          bulk_wait_read_all();  // this lane's previous reduce has read its staging row
+          // The two warps of a lane quadrant hold the same 32 rows (one per
+          // lane) and split the columns.  Each stages w * alpha_e * acc of its
+          // columns into the quadrant's full-width rows; then lanes 0-15 of
+          // each warp add one whole row (BN fp32) into its token's row of y
+          // with one bulk reduce-add.
+          // The two warps meet on the quadrant's mbarrier (bounded waits).
+          float* stg_q = reinterpret_cast<float*>(smem + STAGES * Cfg::STAGE_BYTES + q * 32 * Cfg::EPI_PITCH);
+          bulk_wait_read_all();  // this lane's reduce of the last tile has read its row ...
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&quad_bar[q]);
+          if (!mbar_wait(&quad_bar[q], quad_phase, &abort_flag, p.status)) break;  // ... and so has the partner's
+          quad_phase ^= 1;
           if (rm >= 0) {
             const float scale = row_scale;
+            float* stg = stg_q + lane * (Cfg::EPI_PITCH / 4) + part * COLS;
 #pragma unroll
             for (int c = 0; c < COLS / 32; ++c)
 #pragma unroll
@@ -508,10 +519,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 reinterpret_cast<float4*>(stg + 32 * c)[v] =
                     make_float4(__uint_as_float(r[c][4 * v]) * scale, __uint_as_float(r[c][4 * v + 1]) * scale,
                                 __uint_as_float(r[c][4 * v + 2]) * scale, __uint_as_float(r[c][4 * v + 3]) * scale);
-            fence_proxy_async_smem();
-            bulk_reduce_add_f32(p.y + static_cast<int64_t>(rm / p.topk) * p.ldy + nt * BN + part * COLS, stg,
-                                COLS * 4);
           }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&quad_bar[q]);
+          if (!mbar_wait(&quad_bar[q], quad_phase, &abort_flag, p.status)) break;  // both halves are staged
+          quad_phase ^= 1;
+          const int rr = 16 * part + (lane & 15);
+          const int rm_r = __shfl_sync(0xFFFFFFFFu, rm, rr);
+          if (lane < 16 && rm_r >= 0)
+            bulk_reduce_add_f32(p.y + static_cast<int64_t>(rm_r / p.topk) * p.ldy + nt * BN,
+                                stg_q + rr * (Cfg::EPI_PITCH / 4), BN * 4);
         }
       } else {
         // accumulator columns [0, 128) = gate, [128, 256) = up; this warp owns
