@@ -221,15 +221,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
   }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  // Launched with programmatic serialization: the setup above overlaps the
+  // preceding kernel; nothing it writes (tile counts, tables, operands, the
+  // output global) is read before this point, and nothing it reads is
+  // written.
+  pdl_wait();
+  pdl_launch_dependents();
   if constexpr (MODE == kEpiGatedQuant) {
     if (threadIdx.x < 256) {
       const float S = e4m3_to_f32(threadIdx.x);
       r_of_s8[threadIdx.x] = (S != 0.0f && S == S) ? __fdiv_rn(__ldg(p.g_out), S) : 0.0f;
     }
-  }
-  if (warp == 1) {
-    tmem_alloc(&tmem_slot, Cfg::TMEM_COLS);
-    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -958,8 +964,8 @@ static cudaError_t launch_cfg(const GemmMaps& maps, const GemmParams& p, int gri
   cudaError_t e = cudaFuncSetAttribute(gemm_nvfp4_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  gemm_nvfp4_kernel<Cfg><<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(maps.a, maps.b, p);
-  return cudaGetLastError();
+  return launch_pdl(gemm_nvfp4_kernel<Cfg>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), Cfg::SMEM_BYTES,
+                    stream, maps.a, maps.b, p);
 }
 
 cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {

@@ -30,6 +30,8 @@ constexpr int kIdBatch = 8;  // global loads a thread keeps in flight in the ali
 // Per chunk of `chunk` routes: routes per expert.
 __global__ void __launch_bounds__(256) moe_hist_kernel(const int32_t* __restrict__ ids, int64_t R, int E, int chunk,
                                                        int32_t* __restrict__ hist, int* status) {
+  pdl_wait();  // the routes, tables or buffers of the preceding kernels
+  pdl_launch_dependents();
   extern __shared__ int32_t sh[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
   __syncthreads();
@@ -59,6 +61,8 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ hi
                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                         int32_t* __restrict__ n_tiles, int32_t* __restrict__ row_map,
                                                         int32_t* __restrict__ tile_expert) {
+  pdl_wait();  // the routes, tables or buffers of the preceding kernels
+  pdl_launch_dependents();
   __shared__ int32_t part_s[1024];  // [run][expert] chunk sums
   __shared__ int32_t off_s[1024];   // [expert] padded segment start
   __shared__ int32_t cnt_s[1024];   // [expert] routes
@@ -143,6 +147,8 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ hi
 __global__ void __launch_bounds__(32) moe_scatter_kernel(const int32_t* __restrict__ ids, int64_t R, int E, int chunk,
                                                          const int32_t* __restrict__ hist,
                                                          int32_t* __restrict__ row_map, int32_t* __restrict__ pos) {
+  pdl_wait();  // the routes, tables or buffers of the preceding kernels
+  pdl_launch_dependents();
   extern __shared__ int32_t run[];
   for (int e = threadIdx.x; e < E; e += 32) run[e] = hist[static_cast<int64_t>(blockIdx.x) * E + e];
   __syncwarp();
@@ -192,6 +198,8 @@ __global__ void __launch_bounds__(1024) moe_align_block_kernel(const int32_t* __
                                                                int32_t* __restrict__ row_map,
                                                                int32_t* __restrict__ tile_expert,
                                                                int32_t* __restrict__ pos, int* status) {
+  pdl_wait();  // the routes, tables or buffers of the preceding kernels
+  pdl_launch_dependents();
   extern __shared__ int32_t wh[];  // [32][E]
   __shared__ int32_t warp_sums[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -289,6 +297,8 @@ __global__ void __launch_bounds__(256) moe_quant_permute_kernel(const uint16_t* 
                                                                 uint8_t* __restrict__ a_codes,
                                                                 uint8_t* __restrict__ a_sf, int64_t cpad4,
                                                                 float* __restrict__ y) {
+  pdl_wait();  // the routes, tables or buffers of the preceding kernels
+  pdl_launch_dependents();
   const float g = __ldg(d_g);
   const int lane = threadIdx.x & 31;
   // T * chunks < 2^31 (checked by the launcher): 32-bit index arithmetic
@@ -355,6 +365,8 @@ __global__ void __launch_bounds__(256) moe_quant_permute_kernel(const uint16_t* 
 
 __global__ void __launch_bounds__(256) moe_finalize_kernel(const float* __restrict__ y, int64_t n,
                                                            uint16_t* __restrict__ out) {
+  pdl_wait();  // y of the down GEMM
+  pdl_launch_dependents();
   for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x * 8) {
     const float4 a = reinterpret_cast<const float4*>(y + i)[0];
@@ -411,19 +423,20 @@ cudaError_t launch_moe_align(const int32_t* ids, int64_t T, int topk, int E, con
                                                  static_cast<int>(smem));
       if (e != cudaSuccess) return e;
     }
-    moe_align_block_kernel<<<1, 1024, smem, stream>>>(
-        ids, R, E, w.counts, w.offsets, w.n_tiles, w.row_map, w.tile_expert, w.pos, status);
-    return cudaGetLastError();
+    return launch_pdl(moe_align_block_kernel, dim3(1), dim3(1024), smem, stream, ids, R, E, w.counts, w.offsets,
+                      w.n_tiles, w.row_map, w.tile_expert, w.pos, status);
   }
   const int64_t chunk = moe_align_chunk(R);
   const int nchunks = static_cast<int>((R + chunk - 1) / chunk);
-  moe_hist_kernel<<<nchunks, 256, E * sizeof(int32_t), stream>>>(ids, R, E, static_cast<int>(chunk), w.hist,
-                                                                  status);
-  moe_scan_kernel<<<1, 1024, 0, stream>>>(w.hist, nchunks, E, w.counts, w.offsets, w.n_tiles, w.row_map,
-                                          w.tile_expert);
-  moe_scatter_kernel<<<nchunks, 32, E * sizeof(int32_t), stream>>>(ids, R, E, static_cast<int>(chunk), w.hist,
-                                                                   w.row_map, w.pos);
-  return cudaGetLastError();
+  const int ci = static_cast<int>(chunk);
+  cudaError_t e = launch_pdl(moe_hist_kernel, dim3(nchunks), dim3(256), E * sizeof(int32_t), stream, ids, R, E, ci,
+                             w.hist, status);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(moe_scan_kernel, dim3(1), dim3(1024), 0, stream, w.hist, nchunks, E, w.counts, w.offsets, w.n_tiles,
+                 w.row_map, w.tile_expert);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(moe_scatter_kernel, dim3(nchunks), dim3(32), E * sizeof(int32_t), stream, ids, R, E, ci,
+                    static_cast<const int32_t*>(w.hist), w.row_map, w.pos);
 }
 
 cudaError_t launch_moe_quant_permute(const void* x, int64_t T, int64_t H, int topk, const float* d_g,
@@ -434,9 +447,9 @@ cudaError_t launch_moe_quant_permute(const void* x, int64_t T, int64_t H, int to
   const int64_t cap = static_cast<int64_t>(num_sms) * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  moe_quant_permute_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-      static_cast<const uint16_t*>(x), T, H, topk, d_g, w.pos, w.a1_codes, w.a1_sf, (H / 16 + 3) / 4, w.y);
-  return cudaGetLastError();
+  return launch_pdl(moe_quant_permute_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                    static_cast<const uint16_t*>(x), T, H, topk, d_g, static_cast<const int32_t*>(w.pos), w.a1_codes,
+                    w.a1_sf, static_cast<int64_t>((H / 16 + 3) / 4), w.y);
 }
 
 cudaError_t launch_moe_finalize(const float* y, int64_t n, void* out, int num_sms, cudaStream_t stream) {
@@ -444,8 +457,8 @@ cudaError_t launch_moe_finalize(const float* y, int64_t n, void* out, int num_sm
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  moe_finalize_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(y, n, static_cast<uint16_t*>(out));
-  return cudaGetLastError();
+  return launch_pdl(moe_finalize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, y, n,
+                    static_cast<uint16_t*>(out));
 }
 
 cudaError_t launch_moe_dense_ids(int32_t* ids, int64_t Tc, int E, cudaStream_t stream) {

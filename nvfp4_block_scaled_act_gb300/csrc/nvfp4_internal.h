@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace nvfp4 {
 
 // ---- quantisation (quant.cu) ----------------------------------------------
@@ -23,6 +25,26 @@ enum EpiMode : int { kEpiDense = 0, kEpiGatedQuant = 1, kEpiGatedAmax = 2, kEpiD
 // 128 x 128 tiles (twice the CTAs of the pair kernel's 256 x 256 tiles, a
 // deeper stage ring), dense epilogue.
 constexpr int kLaunchDenseSmall = 4;
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while its predecessor in the stream is still running, and every such kernel
+// executes pdl_wait (griddepcontrol.wait) before it reads or writes memory the
+// predecessors use.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct GemmParams {
   const uint8_t* sfa;      // swizzled scales of A (over all A rows)
