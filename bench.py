@@ -829,6 +829,21 @@ def run_profile(stage: str, reps: int):
         for _ in range(reps):
             nv.nvfp4_moe_w4a4(mc.x, mc.topk_ids, mc.topk_w, g1, Wm.w13_codes, Wm.w13_sf, a13, g2, Wm.w2_codes,
                               Wm.w2_sf, a2, E, I, out=out, workspace=ws)
+    elif stage == "moe_large":
+        cfg = synthdata.MOE_LARGE
+        E, H, I, topk = cfg["E"], cfg["H"], cfg["I"], cfg["topk"]
+        T = 8192
+        mc = synthdata.moe_case(T, E, H, I, topk, cfg["skewed"], seed=0, device=dev)
+        Wm = nv.quantize_moe_weights(lambda e: mc.w13(e), lambda e: mc.w2(e), E, H, I, dev)
+        g1 = nv.nvfp4_compute_global(mc.x_calib)
+        a13 = nv.nvfp4_make_alpha(g1, Wm.g13)
+        g2, _ = nv.nvfp4_moe_calibrate(mc.x_calib, g1, Wm.w13_codes, Wm.w13_sf, a13, E, I)
+        a2 = nv.nvfp4_make_alpha(g2, Wm.g2)
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(nv.nvfp4_moe_workspace(T, H, I, E, topk), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            nv.nvfp4_moe_w4a4(mc.x, mc.topk_ids, mc.topk_w, g1, Wm.w13_codes, Wm.w13_sf, a13, g2, Wm.w2_codes,
+                              Wm.w2_sf, a2, E, I, out=out, workspace=ws)
     elif stage == "moe16":
         cfg = synthdata.MOE_SMALL
         E, H, I, topk = cfg["E"], cfg["H"], cfg["I"], cfg["topk"]
@@ -856,7 +871,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-config sweep after the timed steps")
-    ap.add_argument("--profile", choices=["gemm", "quant", "gemv", "moe", "moe16"],
+    ap.add_argument("--profile", choices=["gemm", "quant", "gemv", "moe", "moe_large", "moe16"],
                     help="launch one stage a few times on a small case (for ncu), print nothing else")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
