@@ -271,11 +271,16 @@ nvfp4_status nvfp4_moe_w4a16(const void* x_bf16, int64_t T, int64_t H, int64_t I
  *   h_codes     u8 [P_max, I/2]   quantised SiLU(gate) * up
  *   h_sf        swizzled over P_max rows
  *   y           fp32 [T, H]       top-k sum before the bf16 rounding
- * P_max = T * topk + E * 127, rounded up to 128. */
+ * row_block: the multiple of rows nvfp4_moe_w4a4 pads each expert's segment
+ * to: 256 when T * topk >= 1024 * E and H % 256 == 0 (the grouped GEMMs then
+ * run on CTA pairs whose 256-row tiles belong to one expert), else 128.
+ * P_max = T * topk + E * (row_block - 1), rounded up to row_block.
+ * nvfp4_moe_calibrate pads to 128 rows in a workspace of this layout. */
 typedef struct {
   size_t counts, offsets, n_tiles, row_map, tile_expert, pos;
   size_t a1_codes, a1_sf, h_codes, h_sf, y, hist, total;
   int64_t p_max;
+  int64_t row_block;
 } nvfp4_moe_layout;
 
 nvfp4_status nvfp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int topk,

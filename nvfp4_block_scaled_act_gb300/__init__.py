@@ -44,7 +44,7 @@ _ST = ctypes.c_int  # nvfp4_status
 class MoELayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "counts", "offsets", "n_tiles", "row_map", "tile_expert", "pos", "a1_codes", "a1_sf",
-        "h_codes", "h_sf", "y", "hist", "total")] + [("p_max", ctypes.c_int64)]
+        "h_codes", "h_sf", "y", "hist", "total")] + [("p_max", ctypes.c_int64), ("row_block", ctypes.c_int64)]
 
 
 # name -> (restype, argtypes); the exported symbols of include/nvfp4.h

@@ -121,10 +121,12 @@ bool make_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int6
 MoELayoutBytes moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk) {
   MoELayoutBytes L{};
   const int64_t R = T * topk;
-  const int64_t p_max = (R + E * 127 + 127) / 128 * 128;
+  const int bm = moe_row_block(T, H, E, topk);
+  const int64_t p_max = (R + E * (bm - 1) + bm - 1) / bm * bm;
   const int64_t chunk = nvfp4::moe_align_chunk(R);
   const int64_t nchunks = (R + chunk - 1) / chunk;
   L.p_max = p_max;
+  L.bm = bm;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -167,6 +169,7 @@ MoEWorkspace moe_carve(void* base, const MoELayoutBytes& L) {
   w.h_sf = b + L.h_sf;
   w.y = reinterpret_cast<float*>(b + L.y);
   w.p_max = L.p_max;
+  w.bm = L.bm;
   return w;
 }
 
@@ -175,7 +178,7 @@ static nvfp4_status launch_grouped(int mode, const uint8_t* a_codes, const uint8
                                    const uint8_t* b_codes, const uint8_t* b_sf, int64_t b_rows_per_expert, int64_t E,
                                    int64_t n_tiles, const MoEWorkspace& w, GemmParams p, const DeviceInfo* dev,
                                    cudaStream_t stream) {
-  GemmMaps maps;
+  GemmMaps maps = {};
   if (!make_codes_map(&maps.a, a_codes, p_max, K / 2)) return NVFP4_ERR_CUDA;
   if (!make_codes_map(&maps.b, b_codes, E * b_rows_per_expert, K / 2)) return NVFP4_ERR_CUDA;
   p.sfa = a_sf;
@@ -190,6 +193,15 @@ static nvfp4_status launch_grouped(int mode, const uint8_t* a_codes, const uint8
   p.b_rows_per_expert = static_cast<int>(b_rows_per_expert);
   p.b_rows_total = static_cast<int>(E * b_rows_per_expert);
   p.status = dev->status;
+  if (w.bm == 256 && (mode == kEpiGatedQuant || mode == kEpiDownSum)) {
+    // CTA pairs on 256-row tiles of one expert; down then covers 256 columns
+    // per tile (H % 256 == 0 when the layout pads to 256)
+    if (mode == kEpiDownSum) p.n_tiles = static_cast<int>(n_tiles / 2);
+    const int64_t pair_tiles = (p_max / 256) * p.n_tiles;
+    const int64_t pairs = pair_tiles < dev->sms / 2 ? (pair_tiles < 1 ? 1 : pair_tiles) : dev->sms / 2;
+    return cuda_status(launch_gemm(mode == kEpiGatedQuant ? kLaunchPairGated : kLaunchPairDown, maps, p,
+                                   static_cast<int>(2 * pairs), stream));
+  }
   const int64_t tiles_max = (p_max / 128) * n_tiles;
   const int grid = static_cast<int>(tiles_max < dev->sms ? (tiles_max < 1 ? 1 : tiles_max) : dev->sms);
   return cuda_status(launch_gemm(mode, maps, p, grid, stream));
@@ -384,6 +396,7 @@ nvfp4_status nvfp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t
   out->hist = L.hist;
   out->total = L.total;
   out->p_max = L.p_max;
+  out->row_block = L.bm;
   return NVFP4_OK;
 }
 
@@ -416,7 +429,7 @@ nvfp4_status nvfp4_moe_w4a4(const void* x, int64_t T, int64_t H, int64_t I, int6
   const DeviceInfo* dev = device_info();
   if (!dev) return NVFP4_ERR_NO_DEVICE;
   const MoEWorkspace w = moe_carve(workspace, L);
-  cudaError_t e = launch_moe_align(topk_ids, T, topk, static_cast<int>(E), w, dev->status, stream);
+  cudaError_t e = launch_moe_align(topk_ids, T, topk, static_cast<int>(E), L.bm, w, dev->status, stream);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
   e = launch_moe_quant_permute(x, T, H, topk, d_g_a1, w, dev->sms, stream);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
@@ -544,7 +557,8 @@ nvfp4_status nvfp4_moe_calibrate(const void* x_calib, int64_t Tc, int64_t H, int
   const MoEWorkspace w = moe_carve(workspace, L);
   cudaError_t e = launch_moe_dense_ids(w.ids, Tc, static_cast<int>(E), stream);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
-  e = launch_moe_align(w.ids, Tc, static_cast<int>(E), static_cast<int>(E), w, dev->status, stream);
+  // 128-row segments: the calibration GEMM runs on single CTAs
+  e = launch_moe_align(w.ids, Tc, static_cast<int>(E), static_cast<int>(E), 128, w, dev->status, stream);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;
   e = launch_moe_quant_permute(x_calib, Tc, H, static_cast<int>(E), d_g_a1, w, dev->sms, stream);
   if (e != cudaSuccess) return NVFP4_ERR_CUDA;

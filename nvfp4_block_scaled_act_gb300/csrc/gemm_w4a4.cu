@@ -126,6 +126,7 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const float* ss
       : "memory");
 }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -156,6 +157,43 @@ __device__ __forceinline__ void quant64(const float (&h)[64], float g, const flo
   }
   c0 = make_uint4(words[0], words[1], words[2], words[3]);
   c1 = make_uint4(words[4], words[5], words[6], words[7]);
+}
+
+// Gated epilogue of one row and 64 h columns: h = silu(a * G) * (a * U) from
+// the gate and up accumulator columns (g0 g1 | u0 u1), then either the NVFP4
+// codes and scales of h at permuted row prow, h columns 64 * hcb .. (quant),
+// or the row's max |h| folded into the expert's amax (calibration).
+template <int MODE>
+__device__ __forceinline__ void gated_row64(const uint32_t (&g0)[32], const uint32_t (&g1)[32],
+                                            const uint32_t (&u0)[32], const uint32_t (&u1)[32], float a, int rm,
+                                            int e, int prow, int hcb, const GemmParams& p, const float* r_of_s8,
+                                            float g_out) {
+  float h[64];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    h[i] = __fmul_rn(silu_f32(__fmul_rn(a, __uint_as_float(g0[i]))), __fmul_rn(a, __uint_as_float(u0[i])));
+    h[32 + i] = __fmul_rn(silu_f32(__fmul_rn(a, __uint_as_float(g1[i]))), __fmul_rn(a, __uint_as_float(u1[i])));
+  }
+  if constexpr (MODE == kEpiGatedQuant) {
+    if (rm >= 0) {
+      uint4 c0, c1;
+      uint32_t s4;
+      quant64(h, g_out, r_of_s8, c0, c1, s4);
+      uint8_t* dst = p.q_codes + static_cast<int64_t>(prow) * p.q_row_bytes + hcb * 32;
+      reinterpret_cast<uint4*>(dst)[0] = c0;
+      reinterpret_cast<uint4*>(dst)[1] = c1;
+      *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(prow, static_cast<int64_t>(hcb) * 4, p.q_cpad4)) = s4;
+    }
+  } else {
+    float m = 0.0f;
+    if (rm >= 0) {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(h[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31) == 0 && m > 0.0f) atomicMax(p.amax + e, __float_as_uint(m));
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -549,36 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acce_bar[acc]);
-        const int prow = mt * 128 + row;
-        const float a = row_scale;
-        float h[64];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          h[i] = __fmul_rn(silu_f32(__fmul_rn(a, __uint_as_float(g0[i]))), __fmul_rn(a, __uint_as_float(u0[i])));
-          h[32 + i] =
-              __fmul_rn(silu_f32(__fmul_rn(a, __uint_as_float(g1[i]))), __fmul_rn(a, __uint_as_float(u1[i])));
-        }
-        if constexpr (MODE == kEpiGatedQuant) {
-          if (rm >= 0) {
-            uint4 c0, c1;
-            uint32_t s4;
-            quant64(h, g_out, r_of_s8, c0, c1, s4);
-            uint8_t* dst = p.q_codes + static_cast<int64_t>(prow) * p.q_row_bytes + nt * 64 + part * 32;
-            reinterpret_cast<uint4*>(dst)[0] = c0;
-            reinterpret_cast<uint4*>(dst)[1] = c1;
-            const int64_t c = static_cast<int64_t>(nt) * 8 + part * 4;
-            *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(prow, c, p.q_cpad4)) = s4;
-          }
-        } else {
-          float m = 0.0f;
-          if (rm >= 0) {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(h[i]));
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-          if (lane == 0 && m > 0.0f) atomicMax(p.amax + e, __float_as_uint(m));
-        }
+        gated_row64<MODE>(g0, g1, u0, u1, row_scale, rm, e, mt * 128 + row, 2 * nt + part, p, r_of_s8, g_out);
       }
       if (++acc == NUM_ACC) {
         acc = 0;
@@ -620,29 +629,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 //               it has been read
 // Each CTA's copies complete on its own full barrier; CTA 0's MMA commits are
 // multicast to the stage-empty and accumulator-full barriers of both CTAs.
-struct PairCfg {
-  static constexpr int STAGES = 5;
+//
+// The grouped MoE GEMMs run on the same pairs when every expert's segment is
+// padded to 256 rows, so that both 128-row halves of a pair tile belong to one
+// expert and share its B tile:
+//   gate_up  N = 256 = 128 gate rows (CTA 0's B half) + the 128 matching up
+//            rows (CTA 1's), so each CTA's accumulator holds G and U of its
+//            rows and runs the gated epilogue of gemm_nvfp4_kernel;
+//   down     N = 256 weight rows; each epilogue warp adds its 32 rows x 128
+//            columns into y in four 32-column slabs (two staging buffers per
+//            warp, one 128-byte bulk reduce-add per row and slab).
+template <int MODE>
+struct PairCfgT {
+  static constexpr bool GROUPED = MODE != kEpiDense;
+  static constexpr int STAGES = MODE == kEpiDownSum ? 4 : 5;
   static constexpr int BN = 256;
   static constexpr int A_BYTES = 128 * 128;   // 128 rows x 256 k
   static constexpr int B_BYTES = 128 * 128;   // this CTA's 128 B rows
   static constexpr int SFA_BYTES = 2048;
   static constexpr int SFB_BYTES = 4096;      // scale atoms of all 256 B rows
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int EPI_WARP_BYTES = 32 * 128;  // one box of 32 rows x 64 bf16 at a time
+  // dense: one box of 32 rows x 64 bf16 at a time; down: two fp32 slabs of
+  // 32 rows x 32 columns (row pitch 144 bytes: the row-per-lane stores of a
+  // quarter-warp fall on distinct banks)
+  static constexpr int DOWN_PITCH = 32 * 4 + 16;
+  static constexpr int EPI_WARP_BYTES =
+      MODE == kEpiDense ? 32 * 128 : (MODE == kEpiDownSum ? 2 * 32 * DOWN_PITCH : 0);
   static constexpr int EPI_BYTES = kNumEpi * EPI_WARP_BYTES;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024;
   static constexpr int SF_COLS = 48;          // TMEM scale columns per stage: 16 (A) + 32 (B)
   static constexpr int SF_BASE = BN;
   static constexpr int TMEM_COLS = 512;
   static_assert(SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
-  static_assert(STAGE_BYTES % 1024 == 0 && EPI_WARP_BYTES % 1024 == 0, "alignment");
+  static_assert(STAGE_BYTES % 1024 == 0 && EPI_WARP_BYTES % 128 == 0, "alignment");
   static_assert(SMEM_BYTES <= 232448, "smem budget");
 };
+using PairCfg = PairCfgT<kEpiDense>;
 
+template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
-  using Cfg = PairCfg;
+  using Cfg = PairCfgT<MODE>;
   constexpr int STAGES = Cfg::STAGES;
   constexpr int BN = Cfg::BN;
 
@@ -656,6 +684,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t done_bar;           // CTA 0: every MMA completed
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
+  __shared__ float r_of_s8[MODE == kEpiGatedQuant ? 256 : 1];  // g_out / S for every E4M3 scale byte
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -676,11 +705,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    prefetch_tmap(&tmOut);
+    if constexpr (MODE == kEpiDense) prefetch_tmap(&tmOut);  // grouped modes pass no output map
   }
   if (warp == 1) {
     tmem_alloc_pair(&tmem_slot, Cfg::TMEM_COLS);
     tmem_relinquish_pair();
+  }
+  if constexpr (Cfg::GROUPED) {
+    // launched with programmatic serialization: the tile count, the tables
+    // and the operands come from the preceding kernels
+    pdl_wait();
+    pdl_launch_dependents();
+    if constexpr (MODE == kEpiGatedQuant) {
+      if (threadIdx.x < 256) {
+        const float S = e4m3_to_f32(threadIdx.x);
+        r_of_s8[threadIdx.x] = (S != 0.0f && S == S) ? __fdiv_rn(__ldg(p.g_out), S) : 0.0f;
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -689,7 +730,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = tmem_slot;
 
   // work units: 256-row tile pairs x 256-column tiles, column-fastest
-  const int m_tiles = p.m_tiles;
+  // (grouped: an even number of 128-row tiles, two per expert pair tile)
+  const int m_tiles = Cfg::GROUPED ? *p.d_m_tiles : p.m_tiles;
   const int total = ((m_tiles + 1) / 2) * p.n_tiles;
   const int unit0 = blockIdx.x >> 1;
   const int unit_step = gridDim.x >> 1;
@@ -710,7 +752,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int mp = tile / p.n_tiles, nt = tile - mp * p.n_tiles;
         const int mt = 2 * mp + static_cast<int>(rank);
         const bool mvalid = mt < m_tiles;
-        const int b_row = nt * BN + 128 * static_cast<int>(rank);
+        // first B row of block j of the pair tile; this CTA copies block `rank`
+        int bj[2];
+        if constexpr (MODE == kEpiDense) {
+          bj[0] = nt * BN;
+          bj[1] = nt * BN + 128;
+        } else {
+          const int e = p.tile_expert[2 * mp];
+          const int base = e * p.b_rows_per_expert;
+          bj[0] = MODE == kEpiDownSum ? base + nt * BN : base + nt * 128;
+          bj[1] = MODE == kEpiDownSum ? base + nt * BN + 128 : base + p.up_offset + nt * 128;
+        }
+        const int b_row = bj[rank];
         for (int kb = 0; kb < p.kblocks; ++kb) {
           const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
           if (!mbar_wait_warp(&empty_bar[stage], phase ^ 1, &abort_flag, p.status)) {
@@ -732,15 +785,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               uint32_t bytes = mvalid ? ks * 512 : 0;
 #pragma unroll
               for (int j = 0; j < 2; ++j)
-                if (nt * BN + 128 * j < p.b_rows_total) bytes += ks * 512;
+                if (bj[j] < p.b_rows_total) bytes += ks * 512;
               mbar_arrive_expect_tx(&full_bar[stage], bytes);
               if (mvalid)
                 bulk_load(sSFA, p.sfa + (static_cast<int64_t>(mt) * p.sf_atoms + kb * 4) * 512, ks * 512,
                           &full_bar[stage]);
 #pragma unroll
               for (int j = 0; j < 2; ++j)
-                if (nt * BN + 128 * j < p.b_rows_total)
-                  bulk_load(sSFB + j * 2048, p.sfb + (static_cast<int64_t>(nt * 2 + j) * p.sf_atoms + kb * 4) * 512,
+                if (bj[j] < p.b_rows_total)
+                  bulk_load(sSFB + j * 2048, p.sfb + (static_cast<int64_t>(bj[j] >> 7) * p.sf_atoms + kb * 4) * 512,
                             ks * 512, &full_bar[stage]);
             }
           }
@@ -894,49 +947,104 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* stg = smem + STAGES * Cfg::STAGE_BYTES + ew * Cfg::EPI_WARP_BYTES;
     const uint32_t acce_lead = mapa_shared(&acce_bar, 0);
     pdl_wait();  // alpha (and the output buffer) may belong to the preceding kernel
-    const float alpha = __ldg(p.alpha);
+    const float alpha = MODE == kEpiDense ? __ldg(p.alpha) : 0.0f;
+    const float g_out = MODE == kEpiGatedQuant ? __ldg(p.g_out) : 0.0f;
     uint32_t acc_phase = 0;
     for (int tile = unit0; tile < total; tile += unit_step) {
       const int mp = tile / p.n_tiles, nt = tile - mp * p.n_tiles;
       const int mt = 2 * mp + static_cast<int>(rank);
+      const int row = 32 * q + lane;
+      // routing data of a grouped tile, loaded while the MMAs run
+      int rm = -1, e = 0;
+      float row_scale = 0.0f;
+      if constexpr (Cfg::GROUPED) {
+        rm = p.row_map[mt * 128 + row];
+        e = p.tile_expert[mt];
+        const float ae = __ldg(p.alpha + e);
+        row_scale = (MODE == kEpiDownSum && rm >= 0) ? __fmul_rn(__ldg(p.topk_w + rm), ae) : ae;
+      }
       if (!mbar_wait(&accf_bar, acc_phase, &abort_flag, p.status)) break;
       tc_fence_after();
-      constexpr int COLS = BN / 2;
-      uint32_t r[COLS / 32][32];
-      drain<COLS>(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + part * COLS, r);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(acce_lead);
-      acc_phase ^= 1;
-      if (mt >= m_tiles) continue;  // rows past M (the second half of the last pair)
-      // row `lane` of a 32 x 64 box, 128-byte rows with the 128-byte swizzle
-      // (16-byte chunk j of row r at chunk j ^ (r % 8)); two boxes per tile
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+      if constexpr (MODE == kEpiDense) {
+        constexpr int COLS = BN / 2;
+        uint32_t r[COLS / 32][32];
+        drain<COLS>(t_row + part * COLS, r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(acce_lead);
+        acc_phase ^= 1;
+        if (mt >= m_tiles) continue;  // rows past M (the second half of the last pair)
+        // row `lane` of a 32 x 64 box, 128-byte rows with the 128-byte swizzle
+        // (16-byte chunk j of row r at chunk j ^ (r % 8)); two boxes per tile
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        // this warp's previous box has been read out of the staging buffer
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
-        uint8_t* row = stg + lane * 128;
+        for (int g = 0; g < 2; ++g) {
+          // this warp's previous box has been read out of the staging buffer
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          uint8_t* srow = stg + lane * 128;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t* v = r[2 * g + j / 4] + 8 * (j % 4);
-          uint4 o;
-          o.x = pack_bf16x2(__uint_as_float(v[0]) * alpha, __uint_as_float(v[1]) * alpha);
-          o.y = pack_bf16x2(__uint_as_float(v[2]) * alpha, __uint_as_float(v[3]) * alpha);
-          o.z = pack_bf16x2(__uint_as_float(v[4]) * alpha, __uint_as_float(v[5]) * alpha);
-          o.w = pack_bf16x2(__uint_as_float(v[6]) * alpha, __uint_as_float(v[7]) * alpha);
-          *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = o;
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t* v = r[2 * g + j / 4] + 8 * (j % 4);
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[0]) * alpha, __uint_as_float(v[1]) * alpha);
+            o.y = pack_bf16x2(__uint_as_float(v[2]) * alpha, __uint_as_float(v[3]) * alpha);
+            o.z = pack_bf16x2(__uint_as_float(v[4]) * alpha, __uint_as_float(v[5]) * alpha);
+            o.w = pack_bf16x2(__uint_as_float(v[6]) * alpha, __uint_as_float(v[7]) * alpha);
+            *reinterpret_cast<uint4*>(srow + ((j ^ (lane & 7)) << 4)) = o;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int x = nt * BN + part * COLS + 64 * g, y = mt * 128 + 32 * q;
+            if (x < p.N && y < p.M) tma_store_2d(&tmOut, stg, x, y);
+          }
+          __syncwarp();
         }
-        fence_proxy_async_smem();
+      } else if constexpr (MODE == kEpiDownSum) {
+        // w * alpha_e * acc of this row, columns 128 part .. 128 part + 127, in
+        // four 32-column slabs; slab j stages in buffer j % 2, reused once the
+        // reduce-add two slabs back has read it
+        uint32_t r[4][32];
+        drain<128>(t_row + part * 128, r);
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          const int x = nt * BN + part * COLS + 64 * g, y = mt * 128 + 32 * q;
-          if (x < p.N && y < p.M) tma_store_2d(&tmOut, stg, x, y);
+        if (lane == 0) mbar_arrive_remote(acce_lead);
+        acc_phase ^= 1;
+        float* ydst = p.y + static_cast<int64_t>(rm >= 0 ? rm / p.topk : 0) * p.ldy + nt * BN + part * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          bulk_wait_read_1();
+          float* srow = reinterpret_cast<float*>(stg + (j & 1) * 32 * Cfg::DOWN_PITCH + lane * Cfg::DOWN_PITCH);
+          if (rm >= 0) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              reinterpret_cast<float4*>(srow)[v] =
+                  make_float4(__uint_as_float(r[j][4 * v]) * row_scale, __uint_as_float(r[j][4 * v + 1]) * row_scale,
+                              __uint_as_float(r[j][4 * v + 2]) * row_scale,
+                              __uint_as_float(r[j][4 * v + 3]) * row_scale);
+            fence_proxy_async_smem();
+            bulk_reduce_add_f32(ydst + 32 * j, srow, 32 * 4);
+          }
         }
+      } else {
+        // accumulator columns [0, 128) = gate, [128, 256) = up; this warp owns
+        // h columns [64 * part, 64 * part + 64) of the tile
+        uint32_t g0[32], g1[32], u0[32], u1[32];
+        tmem_ld_32x32b_x32(t_row + 64 * part, g0);
+        tmem_ld_32x32b_x32(t_row + 64 * part + 32, g1);
+        tmem_ld_32x32b_x32(t_row + 128 + 64 * part, u0);
+        tmem_ld_32x32b_x32(t_row + 128 + 64 * part + 32, u1);
+        tmem_ld_wait();
+        tc_fence_before();
         __syncwarp();
+        if (lane == 0) mbar_arrive_remote(acce_lead);
+        acc_phase ^= 1;
+        gated_row64<MODE>(g0, g1, u0, u1, row_scale, rm, e, mt * 128 + row, 2 * nt + part, p, r_of_s8, g_out);
       }
     }
-    if (lane == 0) bulk_wait_all();  // this warp's stores are complete
+    // this warp's stores (dense: lane 0) and reduce-adds (down: every lane) are complete
+    if (MODE == kEpiDownSum || lane == 0) bulk_wait_all();
     __syncwarp();
   }
 
@@ -968,32 +1076,28 @@ static cudaError_t launch_cfg(const GemmMaps& maps, const GemmParams& p, int gri
                     stream, maps.a, maps.b, p);
 }
 
+template <int MODE>
+static cudaError_t launch_pair(const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {
+  using Cfg = PairCfgT<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;  // whole CTA pairs
+  return launch_pdl(gemm_pair_kernel<MODE>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), Cfg::SMEM_BYTES,
+                    stream, maps.a, maps.b, maps.out, p);
+}
+
 cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int grid, cudaStream_t stream) {
   switch (mode) {
-    case kEpiDense: {
-      cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           PairCfg::SMEM_BYTES);
-      if (e != cudaSuccess) return e;
-      if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;  // whole CTA pairs
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(static_cast<unsigned>(grid));
-      cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
-      cfg.stream = stream;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[0].val.programmaticStreamSerializationAllowed = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      return cudaLaunchKernelEx(&cfg, gemm_pair_kernel, maps.a, maps.b, maps.out, p);
-    }
+    case kEpiDense: return launch_pair<kEpiDense>(maps, p, grid, stream);
     case kEpiGatedQuant: return launch_cfg<GatedCfg>(maps, p, grid, stream);
     case kEpiGatedAmax: return launch_cfg<AmaxCfg>(maps, p, grid, stream);
     case kEpiDownSum: return launch_cfg<DownCfg>(maps, p, grid, stream);
     case kLaunchDenseSmall: return launch_cfg<DenseSmallCfg>(maps, p, grid, stream);
+    case kLaunchPairGated: return launch_pair<kEpiGatedQuant>(maps, p, grid, stream);
+    case kLaunchPairDown: return launch_pair<kEpiDownSum>(maps, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
-
 
 }  // namespace nvfp4

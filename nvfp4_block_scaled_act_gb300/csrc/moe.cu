@@ -4,7 +4,9 @@
 // page, section "Changes").
 //
 // align: a stable counting sort of the T * topk routes by expert, each
-// expert's segment padded to a multiple of 128 rows (one GEMM tile).  Up to
+// expert's segment padded to a multiple of bm rows (128: one GEMM tile; 256: a
+// CTA-pair tile, both halves of one expert).  tile_expert and n_tiles count
+// 128-row tiles either way.  Up to
 // 4096 routes one block does it all (moe_align_block_kernel); above that:
 //   moe_hist_kernel     per chunk of routes (256, doubled while there are
 //                       over 512 chunks), routes per expert
@@ -57,7 +59,7 @@ __global__ void __launch_bounds__(256) moe_hist_kernel(const int32_t* __restrict
 // the padded counts; each run thread then rewrites its chunks as the expert's
 // base for that chunk (in chunk order) and writes its share of the padding
 // rows and tile entries.
-__global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
+__global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E, int bm,
                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                         int32_t* __restrict__ n_tiles, int32_t* __restrict__ row_map,
                                                         int32_t* __restrict__ tile_expert) {
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ hi
   int32_t cnt = 0;
   if (t < E)
     for (int q = 0; q < P; ++q) cnt += part_s[q * E + t];
-  const int32_t padded = (cnt + 127) / 128 * 128;
+  const int32_t padded = (cnt + bm - 1) / bm * bm;
   // exclusive scan of padded over experts (block-wide)
   int32_t v = padded;
   const int lane = t & 31, w = t >> 5;
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ hi
   }
   __syncthreads();
   if (active) {
-    const int32_t off = off_s[e], ce = cnt_s[e], pe = (ce + 127) / 128 * 128;
+    const int32_t off = off_s[e], ce = cnt_s[e], pe = (ce + bm - 1) / bm * bm;
     int32_t base = off;
     for (int q = 0; q < run; ++q) base += part_s[q * E + e];
     for (int c0 = c_begin; c0 < c_end; c0 += kIdBatch) {
@@ -192,6 +194,7 @@ __global__ void __launch_bounds__(32) moe_scatter_kernel(const int32_t* __restri
 constexpr int64_t kAlignOneBlock = 4096;  // above this, one SM's rank matching is the bound
 
 __global__ void __launch_bounds__(1024) moe_align_block_kernel(const int32_t* __restrict__ ids, int64_t R, int E,
+                                                               int bm,
                                                                int32_t* __restrict__ counts,
                                                                int32_t* __restrict__ offsets,
                                                                int32_t* __restrict__ n_tiles,
@@ -248,7 +251,7 @@ __global__ void __launch_bounds__(1024) moe_align_block_kernel(const int32_t* __
     int32_t cnt = 0;
     if (e < E)
       for (int w = 0; w < 32; ++w) cnt += wh[w * E + e];
-    const int32_t padded = (cnt + 127) / 128 * 128;
+    const int32_t padded = (cnt + bm - 1) / bm * bm;
     int32_t v = padded;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -413,8 +416,8 @@ __global__ void __launch_bounds__(1024) moe_calib_finish_kernel(unsigned int* __
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
-cudaError_t launch_moe_align(const int32_t* ids, int64_t T, int topk, int E, const MoEWorkspace& w, int* status,
-                             cudaStream_t stream) {
+cudaError_t launch_moe_align(const int32_t* ids, int64_t T, int topk, int E, int bm, const MoEWorkspace& w,
+                             int* status, cudaStream_t stream) {
   const int64_t R = T * topk;
   if (R <= kAlignOneBlock && E <= 1024) {
     const size_t smem = 32 * static_cast<size_t>(E) * sizeof(int32_t);
@@ -423,8 +426,8 @@ cudaError_t launch_moe_align(const int32_t* ids, int64_t T, int topk, int E, con
                                                  static_cast<int>(smem));
       if (e != cudaSuccess) return e;
     }
-    return launch_pdl(moe_align_block_kernel, dim3(1), dim3(1024), smem, stream, ids, R, E, w.counts, w.offsets,
-                      w.n_tiles, w.row_map, w.tile_expert, w.pos, status);
+    return launch_pdl(moe_align_block_kernel, dim3(1), dim3(1024), smem, stream, ids, R, E, bm, w.counts,
+                      w.offsets, w.n_tiles, w.row_map, w.tile_expert, w.pos, status);
   }
   const int64_t chunk = moe_align_chunk(R);
   const int nchunks = static_cast<int>((R + chunk - 1) / chunk);
@@ -432,8 +435,8 @@ cudaError_t launch_moe_align(const int32_t* ids, int64_t T, int topk, int E, con
   cudaError_t e = launch_pdl(moe_hist_kernel, dim3(nchunks), dim3(256), E * sizeof(int32_t), stream, ids, R, E, ci,
                              w.hist, status);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(moe_scan_kernel, dim3(1), dim3(1024), 0, stream, w.hist, nchunks, E, w.counts, w.offsets, w.n_tiles,
-                 w.row_map, w.tile_expert);
+  e = launch_pdl(moe_scan_kernel, dim3(1), dim3(1024), 0, stream, w.hist, nchunks, E, bm, w.counts, w.offsets,
+                 w.n_tiles, w.row_map, w.tile_expert);
   if (e != cudaSuccess) return e;
   return launch_pdl(moe_scatter_kernel, dim3(nchunks), dim3(32), E * sizeof(int32_t), stream, ids, R, E, ci,
                     static_cast<const int32_t*>(w.hist), w.row_map, w.pos);

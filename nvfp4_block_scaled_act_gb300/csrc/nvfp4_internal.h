@@ -25,6 +25,9 @@ enum EpiMode : int { kEpiDense = 0, kEpiGatedQuant = 1, kEpiGatedAmax = 2, kEpiD
 // 128 x 128 tiles (twice the CTAs of the pair kernel's 256 x 256 tiles, a
 // deeper stage ring), dense epilogue.
 constexpr int kLaunchDenseSmall = 4;
+// MoE gate_up / down on CTA pairs (expert segments padded to 256 rows)
+constexpr int kLaunchPairGated = 5;
+constexpr int kLaunchPairDown = 6;
 
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while its predecessor in the stream is still running, and every such kernel

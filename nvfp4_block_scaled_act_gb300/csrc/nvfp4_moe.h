@@ -24,13 +24,27 @@ struct MoEWorkspace {
   float* y;              // [T, H]
   unsigned int* amax;    // [E] (calibration)
   int64_t p_max;
+  int bm;  // row block the segments are padded to (256: the grouped GEMMs run on CTA pairs)
 };
 
 struct MoELayoutBytes {
   size_t counts, offsets, n_tiles, row_map, tile_expert, pos, hist, ids, a1_codes, a1_sf, h_codes, h_sf, y, amax,
       total;
   int64_t p_max;
+  int bm;  // row block of the alignment for nvfp4_moe_w4a4 (moe_row_block)
 };
+
+// Row block the W4A4 MoE pads every expert segment to: 256 (the grouped GEMMs
+// then run on CTA pairs, 256-row tiles of one expert) once the experts average
+// at least kPairRoutesPerExpert routes and the hidden size splits into
+// 256-column down tiles; else 128 (one CTA per 128-row tile).  Per padded row
+// the pairs are about 15 % faster, but 256-row padding adds about 64 rows per
+// expert on average: at 256 routes per expert that is 20 % more rows and the
+// pairs lose, at 1024 it is about 6 % and they win.
+constexpr int64_t kPairRoutesPerExpert = 1024;
+inline int moe_row_block(int64_t T, int64_t H, int64_t E, int64_t topk) {
+  return (T * topk >= kPairRoutesPerExpert * E && H % 256 == 0) ? 256 : 128;
+}
 
 // Routes per histogram / scatter chunk of the multi-block align: 256, doubled
 // until there are at most 512 chunks, so the scatter has a warp per 256-512
@@ -45,8 +59,9 @@ inline int64_t moe_align_chunk(int64_t R) {
 MoELayoutBytes moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk);
 MoEWorkspace moe_carve(void* base, const MoELayoutBytes& L);
 
-cudaError_t launch_moe_align(const int32_t* ids, int64_t T, int topk, int E, const MoEWorkspace& w, int* status,
-                             cudaStream_t stream);
+// bm: 128 or 256, the row block every expert segment is padded to
+cudaError_t launch_moe_align(const int32_t* ids, int64_t T, int topk, int E, int bm, const MoEWorkspace& w,
+                             int* status, cudaStream_t stream);
 cudaError_t launch_moe_quant_permute(const void* x, int64_t T, int64_t H, int topk, const float* d_g,
                                      const MoEWorkspace& w, int num_sms, cudaStream_t stream);
 cudaError_t launch_moe_finalize(const float* y, int64_t n, void* out, int num_sms, cudaStream_t stream);

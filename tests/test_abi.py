@@ -82,7 +82,11 @@ def test_no_device_is_reported_without_a_gpu(lib):
 def test_moe_workspace_layout(lib):
     T, H, I, E, topk = 4096, 2048, 768, 128, 8
     lay = nv.nvfp4_moe_workspace_layout(T, H, I, E, topk)
+    assert lay.row_block == 128   # 256 routes per expert on average: 128-row segments
     assert lay.p_max == (T * topk + E * 127 + 127) // 128 * 128
+    big = nv.nvfp4_moe_workspace_layout(4 * T, H, I, E, topk)   # 1024 routes per expert: CTA pairs
+    assert big.row_block == 256 and big.p_max == (4 * T * topk + E * 255 + 255) // 256 * 256
+    assert nv.nvfp4_moe_workspace_layout(4 * T, 1920, I, E, topk).row_block == 128   # H % 256 != 0
     assert lay.total == lib.nvfp4_moe_workspace(T, H, I, E, topk)
     offs = [lay.counts, lay.offsets, lay.n_tiles, lay.row_map, lay.tile_expert, lay.pos, lay.a1_codes,
             lay.a1_sf, lay.h_codes, lay.h_sf, lay.y, lay.hist]

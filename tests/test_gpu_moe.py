@@ -96,8 +96,13 @@ def unswizzle_row(sf: torch.Tensor, r: int, C: int) -> list:
     return [int(sf[oracle.scale_offset(r, c, C)]) for c in range(C)]
 
 
+def row_block(nv, m: MoE) -> int:
+    """The segment padding the layer uses: 256 (CTA-pair GEMMs) or 128."""
+    return int(nv.nvfp4_moe_workspace_layout(m.T, m.H, m.I, m.E, m.topk).row_block)
+
+
 def staged_check(nv, m: MoE, ws, h_mismatch_max=2e-3):
-    ref_al = oracle.moe_align(m.case.topk_ids, m.E, 128)
+    ref_al = oracle.moe_align(m.case.topk_ids, m.E, row_block(nv, m))
     P = ref_al["P"]
     counts = ws_view(nv, ws, m, "counts", torch.int32, m.E)
     offsets = ws_view(nv, ws, m, "offsets", torch.int32, m.E + 1)
@@ -107,7 +112,7 @@ def staged_check(nv, m: MoE, ws, h_mismatch_max=2e-3):
     assert torch.equal(counts, ref_al["counts"])
     assert torch.equal(offsets, ref_al["offsets"])
     assert torch.equal(row_map, ref_al["row_map"])
-    assert torch.equal(tiles, ref_al["tile_expert"])
+    assert torch.equal(tiles, ref_al["tile_expert"].repeat_interleave(row_block(nv, m) // 128))
     assert int(n_tiles[0]) == P // 128
     # permuted activations
     lay = nv.nvfp4_moe_workspace_layout(m.T, m.H, m.I, m.E, m.topk)
@@ -142,7 +147,7 @@ def test_moe_repeatable_layout(nv):
     m = MoE(nv, T=64, E=16, H=256, I=256, topk=8, seed=2)
     o1, ws1 = m.run_gpu(nv)
     o2, ws2 = m.run_gpu(nv)
-    P = oracle.moe_align(m.case.topk_ids, m.E, 128)["P"]
+    P = oracle.moe_align(m.case.topk_ids, m.E, row_block(nv, m))["P"]
     for name, n in (("counts", m.E), ("offsets", m.E + 1), ("n_tiles", 1), ("row_map", P),
                     ("tile_expert", P // 128), ("pos", m.T * m.topk)):
         a = ws_view(nv, ws1, m, name, torch.int32, n)
@@ -150,6 +155,23 @@ def test_moe_repeatable_layout(nv):
         assert torch.equal(a, b), f"{name} differs between runs"
     check_close(o1, m.run_oracle(), "MoE 64 tokens")
     check_close(o2, o1, "run to run", ulps=1.0, rel_l2=1e-5)
+
+
+@pytest.mark.parametrize("T,E,H,I,topk,skewed", [
+    (1024, 4, 256, 128, 4, False),   # 1024 routes per expert: segments padded to 256
+    (2048, 8, 512, 256, 4, True),    # skewed: pair tiles with few real rows
+    (1100, 3, 768, 384, 3, True),    # ragged segments, three 256-column down tiles
+])
+def test_moe_pair_tiles_staged(nv, T, E, H, I, topk, skewed):
+    """Layers whose experts average >= 1024 routes: gate_up and down run on CTA
+    pairs (256-row tiles of one expert); every stage against the oracle on all
+    tokens."""
+    m = MoE(nv, T=T, E=E, H=H, I=I, topk=topk, skewed=skewed, seed=7)
+    assert row_block(nv, m) == 256
+    out, ws = m.run_gpu(nv)
+    assert nv.nvfp4_device_status() == 0
+    staged_check(nv, m, ws)
+    check_close(out, m.run_oracle(), f"MoE pairs T={T} E={E}")
 
 
 @pytest.mark.parametrize("T", [16, 128])

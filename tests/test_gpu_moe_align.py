@@ -2,7 +2,8 @@
 expert, segments padded to 128-row tiles) against the oracle, bit-exact, over
 route counts that take the one-block path and the chunked path (one chunk,
 many chunks, the largest chunks, a ragged last chunk), expert counts from 1 to
-1024 and skewed routing.  The layer runs on placeholder weights: only the
+1024, skewed routing, and both segment paddings (128 rows, and 256 rows where
+the experts average 1024 routes and the grouped GEMMs run on CTA pairs).  The layer runs on placeholder weights: only the
 layout in the workspace is compared, with pos (route -> permuted row) checked
 as the inverse of row_map."""
 import pytest
@@ -13,7 +14,7 @@ import synthdata
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-H = I = 128
+I = 128
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -27,7 +28,7 @@ def nv():
     return m
 
 
-def placeholder_weights(nv, E):
+def placeholder_weights(nv, E, H):
     """Codes of zero and unit scales (E4M3 0x38 = 1.0): every product is 0."""
     w13c = torch.zeros(E * 2 * I, H // 2, dtype=torch.uint8, device=DEV)
     w13s = torch.full((E * nv.nvfp4_scale_bytes(2 * I, H),), 0x38, dtype=torch.uint8, device=DEV)
@@ -41,22 +42,24 @@ def ws_field(nv, ws, lay, name, count):
     return ws[off:off + 4 * count].view(torch.int32).cpu()
 
 
-@pytest.mark.parametrize("T,topk,E,skewed", [
-    (512, 8, 8, False),       # 4096 routes: the one-block path at its limit
-    (600, 8, 8, False),       # just above it: 19 chunks of 256, ragged tail
-    (4097, 1, 5, True),       # 17 chunks, the last holding one route
-    (4096, 8, 128, False),    # 128 chunks, 8 runs per expert column
-    (5000, 1, 1, False),      # one expert: more runs than chunks
-    (3001, 3, 1024, True),    # 1024 experts: one run per column
-    (3000, 4, 1000, False),   # expert count not dividing the block
-    (32768, 8, 256, True),    # 512 chunks of 512 routes
-    (175001, 3, 3, True),     # 2048-route chunks, 257 of them
+@pytest.mark.parametrize("T,topk,E,skewed,H", [
+    (512, 8, 8, False, 128),      # 4096 routes: the one-block path at its limit
+    (2048, 2, 2, False, 256),     # the same with 2048 routes per expert: padded to 256
+    (600, 8, 8, False, 128),      # just above it: 19 chunks of 256, ragged tail
+    (4097, 1, 5, True, 128),      # 17 chunks, the last holding one route
+    (4097, 2, 4, True, 256),      # ... 2048 routes per expert: padded to 256
+    (4096, 8, 128, False, 128),   # 128 chunks, 8 runs per expert column
+    (5000, 1, 1, False, 256),     # one expert: more runs than chunks, padded to 256
+    (3001, 3, 1024, True, 128),   # 1024 experts: one run per column
+    (3000, 4, 1000, False, 128),  # expert count not dividing the block
+    (32768, 8, 256, True, 256),   # 512 chunks of 512 routes, 1024 per expert: padded to 256
+    (175001, 3, 3, True, 256),    # 2048-route chunks, 257 of them
 ])
-def test_align_layout_exact(nv, T, topk, E, skewed):
+def test_align_layout_exact(nv, T, topk, E, skewed, H):
     assert topk <= E
     ids, w = synthdata.routing(T, E, topk, seed=T + E, skewed=skewed)
     x = synthdata.activations(T, H, seed=1).to(torch.bfloat16)
-    w13c, w13s, w2c, w2s = placeholder_weights(nv, E)
+    w13c, w13s, w2c, w2s = placeholder_weights(nv, E, H)
     one = torch.ones(1, dtype=torch.float32, device=DEV)
     alphas = torch.ones(E, dtype=torch.float32, device=DEV)
     ws = torch.empty(nv.nvfp4_moe_workspace(T, H, I, E, topk), dtype=torch.uint8, device=DEV)
@@ -66,15 +69,19 @@ def test_align_layout_exact(nv, T, topk, E, skewed):
     assert nv.nvfp4_device_status() == 0
     assert torch.count_nonzero(out).item() == 0
 
-    ref = oracle.moe_align(ids, E, 128)
-    P = ref["P"]
     lay = nv.nvfp4_moe_workspace_layout(T, H, I, E, topk)
+    bm = int(lay.row_block)
+    assert bm == (256 if T * topk >= 1024 * E and H % 256 == 0 else 128)
+    ref = oracle.moe_align(ids, E, bm)
+    P = ref["P"]
     assert torch.equal(ws_field(nv, ws, lay, "counts", E), ref["counts"])
     assert torch.equal(ws_field(nv, ws, lay, "offsets", E + 1), ref["offsets"])
     assert int(ws_field(nv, ws, lay, "n_tiles", 1)[0]) == P // 128
     row_map = ws_field(nv, ws, lay, "row_map", P)
     assert torch.equal(row_map, ref["row_map"])
-    assert torch.equal(ws_field(nv, ws, lay, "tile_expert", P // 128), ref["tile_expert"])
+    # one entry per 128-row tile on the device; the oracle has one per bm-row tile
+    assert torch.equal(ws_field(nv, ws, lay, "tile_expert", P // 128),
+                       ref["tile_expert"].repeat_interleave(bm // 128))
     pos = ws_field(nv, ws, lay, "pos", T * topk)
     real = (row_map >= 0).nonzero().flatten()
     assert real.numel() == T * topk
