@@ -174,6 +174,11 @@ MoEWorkspace moe_carve(void* base, const MoELayoutBytes& L) {
 }
 
 // grouped GEMM launch over the permuted rows of the MoE workspace
+// Up to this many routes per expert on average, MoE down adds its rows into y
+// with vector reductions from registers (kEpiDownDirect) instead of staged
+// 512-byte bulk reduce-adds (kEpiDownSum).
+constexpr int64_t kDirectDownRoutesPerExpert = 32;
+
 static nvfp4_status launch_grouped(int mode, const uint8_t* a_codes, const uint8_t* a_sf, int64_t p_max, int64_t K,
                                    const uint8_t* b_codes, const uint8_t* b_sf, int64_t b_rows_per_expert, int64_t E,
                                    int64_t n_tiles, const MoEWorkspace& w, GemmParams p, const DeviceInfo* dev,
@@ -453,8 +458,10 @@ nvfp4_status nvfp4_moe_w4a4(const void* x, int64_t T, int64_t H, int64_t I, int6
     p.ldy = H;
     p.topk_w = topk_w;
     p.topk = topk;
-    st = launch_grouped(kEpiDownSum, w.h_codes, w.h_sf, w.p_max, I, w2_codes, w2_sf, H, E, H / 128, w, p, dev,
-                        stream);
+    // few routes per expert: the tile loop is bound by the weight stream, and
+    // the register-direct top-k adds free the staging memory for 6 stages
+    const int down = T * topk <= kDirectDownRoutesPerExpert * E ? kEpiDownDirect : kEpiDownSum;
+    st = launch_grouped(down, w.h_codes, w.h_sf, w.p_max, I, w2_codes, w2_sf, H, E, H / 128, w, p, dev, stream);
     if (st != NVFP4_OK) return st;
   }
   return cuda_status(launch_moe_finalize(w.y, T * H, out, dev->sms, stream));

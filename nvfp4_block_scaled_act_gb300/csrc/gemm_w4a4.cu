@@ -9,8 +9,9 @@
 //   kEpiGatedQuant h = silu(alpha_e * G) * (alpha_e * U) -> NVFP4 codes/scales
 //                  (MoE gate_up: B tile = 128 gate rows then 128 up rows)
 //   kEpiGatedAmax  per-expert max |h| (calibration of the second input global)
-//   kEpiDownSum    y[t] += w_route * alpha_e * acc with fp32 vector reductions
-//                  (MoE down and top-k sum)
+//   kEpiDownSum    y[t] += w_route * alpha_e * acc with fp32 bulk reductions
+//                  (MoE down and top-k sum); kEpiDownDirect the same with
+//                  vector reductions from registers, for few routes per expert
 // The W4A4 linear of "run nvfp4 linears on nvfp4 activations on sm_120" and the
 // warp-specialised gate_up / down GEMMs of the W4A4 MoE prefill page (both
 // section "Changes") were written for mma.sync on sm_120; this kernel keeps
@@ -64,7 +65,7 @@ struct GemmCfg {
   // MoE down: fp32 staging of the 128 rows x BN columns of a tile (row pitch
   // padded by 16 bytes) for the bulk reduce-adds into y
   static constexpr int EPI_PITCH = BN * 4 + 16;
-  static constexpr int EPI_BYTES = MODE_ == 3 ? 128 * EPI_PITCH : 0;
+  static constexpr int EPI_BYTES = MODE_ == kEpiDownSum ? 128 * EPI_PITCH : 0;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024;
   static constexpr int SF_COLS = 16 + 4 * (BN / 32);  // TMEM scale columns per stage
   static constexpr int SF_BASE = NUM_ACC * BN;
@@ -88,9 +89,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
+__device__ __forceinline__ void red_add_v2(float* addr, float a, float b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1,%2};" ::"l"(addr), "f"(a), "f"(b) : "memory");
 }
 
 // 32 fp32 accumulator values * alpha -> bf16, stored as four 16-byte vectors;
@@ -109,12 +109,6 @@ __device__ __forceinline__ void store_bf16_32(uint16_t* dst, const uint32_t (&r)
   }
 }
 
-__device__ __forceinline__ void red_add_32(float* dst, const uint32_t (&r)[32], float scale) {
-#pragma unroll
-  for (int v = 0; v < 8; ++v)
-    red_add_v4(dst + 4 * v, __uint_as_float(r[4 * v]) * scale, __uint_as_float(r[4 * v + 1]) * scale,
-               __uint_as_float(r[4 * v + 2]) * scale, __uint_as_float(r[4 * v + 3]) * scale);
-}
 
 // Bulk reduce-add of `bytes` fp32 from shared memory into global memory
 // (both 16-byte aligned, bytes % 16 == 0), in this thread's bulk group.
@@ -513,7 +507,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // per-row routing data of a grouped tile, loaded while the MMAs run
       int rm = -1, e = 0;
       float row_scale = 0.0f;
-      if constexpr (Cfg::GROUPED) {
+      // kEpiDownDirect: the four rows this thread adds (16x256b layout, below)
+      int drm[4] = {-1, -1, -1, -1};
+      float dsc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if constexpr (MODE == kEpiDownDirect) {
+        e = p.tile_expert[mt];
+        const float ae = __ldg(p.alpha + e);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          drm[i] = p.row_map[mt * 128 + 32 * q + 16 * (i >> 1) + (lane >> 2) + 8 * (i & 1)];
+          dsc[i] = drm[i] >= 0 ? __fmul_rn(__ldg(p.topk_w + drm[i]), ae) : 0.0f;
+        }
+      } else if constexpr (Cfg::GROUPED) {
         rm = p.row_map[mt * 128 + row];
         e = p.tile_expert[mt];
         const float ae = __ldg(p.alpha + e);
@@ -523,7 +528,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
 
-      if constexpr (MODE == kEpiDense || MODE == kEpiDownSum) {
+      if constexpr (MODE == kEpiDownDirect) {
+        // w * alpha_e * acc of this warp's 32 rows x 64 columns, added into
+        // the tokens' rows of y straight from registers: with the 16x256b
+        // layout four consecutive lanes hold 32 contiguous bytes of one row,
+        // so each red.v2 of the warp covers eight whole 32-byte sectors.
+        // Half hh holds TMEM lanes 32q + 16hh ..; thread t adds rows
+        // 16hh + t/4 (i = 2hh) and 16hh + t/4 + 8 (i = 2hh + 1) of the quadrant.
+        static_assert(BN == 128, "64 columns per epilogue warp");
+        uint32_t v[2][32];
+        tmem_ld_16x256b_x8(t_row + part * 64, v[0]);
+        tmem_ld_16x256b_x8(t_row + (16u << 16) + part * 64, v[1]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce_bar[acc]);
+        const int c0 = nt * BN + part * 64 + 2 * (lane & 3);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (drm[i] >= 0) {
+            float* yrow = p.y + static_cast<int64_t>(drm[i] / p.topk) * p.ldy + c0;
+            const float sc = dsc[i];
+            const uint32_t* vv = v[i >> 1];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              red_add_v2(yrow + 8 * j, __uint_as_float(vv[4 * j + 2 * (i & 1)]) * sc,
+                         __uint_as_float(vv[4 * j + 2 * (i & 1) + 1]) * sc);
+          }
+        }
+      } else if constexpr (MODE == kEpiDense || MODE == kEpiDownSum) {
         // this warp owns COLS accumulator columns: read them all, release the
         // accumulator, then finish from registers
         constexpr int COLS = BN / 2;
@@ -1063,6 +1096,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 using GatedCfg = GemmCfg<256, 1, 4, kEpiGatedQuant>;
 using AmaxCfg = GemmCfg<256, 1, 4, kEpiGatedAmax>;
 using DownCfg = GemmCfg<128, 2, 4, kEpiDownSum>;
+using DownDirectCfg = GemmCfg<128, 2, 6, kEpiDownDirect>;  // 6 x 36 KB stages, no staging
 using DenseSmallCfg = GemmCfg<128, 2, 6, kEpiDense>;  // 6 x 36 KB stages, 2 x 128 + 6 x 32 TMEM columns
 
 template <class Cfg>
@@ -1093,6 +1127,7 @@ cudaError_t launch_gemm(int mode, const GemmMaps& maps, const GemmParams& p, int
     case kEpiGatedQuant: return launch_cfg<GatedCfg>(maps, p, grid, stream);
     case kEpiGatedAmax: return launch_cfg<AmaxCfg>(maps, p, grid, stream);
     case kEpiDownSum: return launch_cfg<DownCfg>(maps, p, grid, stream);
+    case kEpiDownDirect: return launch_cfg<DownDirectCfg>(maps, p, grid, stream);
     case kLaunchDenseSmall: return launch_cfg<DenseSmallCfg>(maps, p, grid, stream);
     case kLaunchPairGated: return launch_pair<kEpiGatedQuant>(maps, p, grid, stream);
     case kLaunchPairDown: return launch_pair<kEpiDownSum>(maps, p, grid, stream);

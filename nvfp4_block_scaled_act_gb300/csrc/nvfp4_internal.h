@@ -20,7 +20,13 @@ cudaError_t launch_make_alpha(const float* d_g_a, const float* d_g_w, int64_t n,
 cudaError_t launch_reduce_max(const float* d_in, int64_t n, float* d_out, cudaStream_t stream);
 
 // ---- block-scaled tcgen05 GEMM (gemm_w4a4.cu) ------------------------------
-enum EpiMode : int { kEpiDense = 0, kEpiGatedQuant = 1, kEpiGatedAmax = 2, kEpiDownSum = 3 };
+enum EpiMode : int {
+  kEpiDense = 0,
+  kEpiGatedQuant = 1,
+  kEpiGatedAmax = 2,
+  kEpiDownSum = 3,     // MoE down: rows staged in shared memory, 512-byte bulk reduce-adds into y
+  kEpiDownDirect = 7,  // MoE down for few routes per expert: vector reductions straight from TMEM reads
+};
 // Launch mode of the dense W4A4 linear for small M: the single-CTA kernel on
 // 128 x 128 tiles (twice the CTAs of the pair kernel's 256 x 256 tiles, a
 // deeper stage ring), dense epilogue.
