@@ -173,12 +173,13 @@ MoEWorkspace moe_carve(void* base, const MoELayoutBytes& L) {
   return w;
 }
 
-// grouped GEMM launch over the permuted rows of the MoE workspace
 // Up to this many routes per expert on average, MoE down adds its rows into y
 // with vector reductions from registers (kEpiDownDirect) instead of staged
 // 512-byte bulk reduce-adds (kEpiDownSum).
 constexpr int64_t kDirectDownRoutesPerExpert = 32;
 
+// grouped GEMM launch over the permuted rows of the MoE workspace; with 256-row
+// segments (w.bm) gate_up and down run on CTA pairs
 static nvfp4_status launch_grouped(int mode, const uint8_t* a_codes, const uint8_t* a_sf, int64_t p_max, int64_t K,
                                    const uint8_t* b_codes, const uint8_t* b_sf, int64_t b_rows_per_expert, int64_t E,
                                    int64_t n_tiles, const MoEWorkspace& w, GemmParams p, const DeviceInfo* dev,

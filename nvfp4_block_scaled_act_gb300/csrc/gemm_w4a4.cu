@@ -257,10 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&tmem_slot, Cfg::TMEM_COLS);
     tmem_relinquish();
   }
-  // Launched with programmatic serialization: the setup above overlaps the
-  // preceding kernel; nothing it writes (tile counts, tables, operands, the
-  // output global) is read before this point, and nothing it reads is
-  // written.
+  // Launched with programmatic serialization: the setup above (barriers, TMEM,
+  // descriptor prefetch) touches no global memory and overlaps the preceding
+  // kernel; tile counts, tables, operands and outputs are accessed only after
+  // this wait.
   pdl_wait();
   pdl_launch_dependents();
   if constexpr (MODE == kEpiGatedQuant) {
