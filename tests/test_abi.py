@@ -70,6 +70,9 @@ def test_quant_and_w4a16_argument_errors(lib):
     assert g(P, 17, 512, P, P, 64, 512, P, P, 64, None, 0, None) == 2   # T > 16
     assert g(P, 4, 512, P, P, 64, 192, P, P, 64, None, 0, None) == 2    # K % 128
     assert g(P, 0, 512, P, P, 64, 512, P, P, 64, None, 0, None) == 0
+    na = lib.nvfp4_linear_w4a16_noalloc
+    assert na(None, 0, 512, None, None, 64, 512, None, None, 64, None) == 0   # T = 0
+    assert na(P, 17, 512, P, P, 64, 512, P, P, 64, None) == 2                # T > 16
 
 
 def test_no_device_is_reported_without_a_gpu(lib):
@@ -94,6 +97,8 @@ def test_moe_workspace_layout(lib):
     assert lay.y + 4 * T * H <= lay.total
     assert lay.h_codes + lay.p_max * I // 2 <= lay.h_sf
     f = lib.nvfp4_moe_w4a4
+    # T = 0: nothing to do, before any pointer is looked at or a device touched
+    assert f(*([None, 0, 2048, 768, 128, 8] + [None] * 12 + [ctypes.c_size_t(0), None])) == 0
     args = [P, 16, 2048, 768, 128, 33] + [P] * 12 + [ctypes.c_size_t(1 << 40), None]
     assert f(*args) == 2   # topk > 32
     args[5] = 8
