@@ -621,7 +621,7 @@ def run_ours(args, world, rank, local):
         # the dominant kernel of the step (most of its device time, by the ncu
         # launch list of this command) is the decode GEMM; its roofline is
         # given for the headline decode call, T = 1 on 8704 x 5120
-        "roofline": {"kernel": "gemv_ring_kernel<0> (W4A16 decode, T=1, 8704x5120)", "bound": "hbm",
+        "roofline": {"kernel": "gemv_ring_kernel<0, 2> (W4A16 decode, T=1, 8704x5120)", "bound": "hbm",
                      "achieved": round(head["gbs"], 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(head["gbs"] / hbm, 4),
                      "peak_source": f"{peak_src} copy bandwidth",

@@ -240,9 +240,10 @@ __global__ void __launch_bounds__(256) gemv_reduce_kernel(const float* __restric
 // L2, before the kernel waits for the preceding kernel on the stream
 // (programmatic dependent launch); the producer refills slots as the compute
 // warps release them.  A call has one CTA per SM at most (the cluster size is
-// the number of SMs over the row blocks) and a CTA takes under half of an
-// SM's shared memory and registers, so the next call's CTAs are resident
-// while this call computes and their weight copies overlap it.
+// the number of SMs over the row blocks).  Below four tokens a CTA takes
+// under half of an SM's shared memory and registers, so the next call's CTAs
+// are resident while this call computes and their weight copies overlap it;
+// from four tokens a CTA takes the whole SM (see RingShape).
 //
 // Activations.  After the dependency wait the compute warps stage the CTA's
 // k-range of the T tokens as f16: each (token, 128-k block) is rescaled by its
@@ -252,8 +253,8 @@ __global__ void __launch_bounds__(256) gemv_reduce_kernel(const float* __restric
 // exactly; smaller values round on the f16 subnormal grid, an error below
 // 2^-39 of the maximum.
 //
-// Arithmetic.  Sixteen compute warps: eight 16-row tiles x two k-groups (the
-// 128-k blocks are dealt to the groups round-robin).  mma.sync.m16n8k16 with
+// Arithmetic.  Sixteen or twenty-four compute warps: eight 16-row tiles x two
+// or three k-groups (the 128-k blocks are dealt to the groups round-robin).  mma.sync.m16n8k16 with
 // 16 weight rows as A and 8 tokens as B (tokens 8..15 in a second MMA), each
 // 128-k block into a fresh fp32 accumulator that is then added, times the
 // block's inverse rescale (a power of two, exact), to the running sums.
@@ -264,8 +265,8 @@ __global__ void __launch_bounds__(256) gemv_reduce_kernel(const float* __restric
 // at most 6 significant bits and lies in [2^-10, 2688], so it is exact in
 // f16, and products of f16 values are exact in fp32.
 //
-// Split-K sum.  The two k-groups add their partials in shared memory in a
-// fixed order.  Rank r of the cluster owns rows [r * rows_per, ...) of the
+// Split-K sum.  The k-groups add their partials in shared memory in a fixed
+// order.  Rank r of the cluster owns rows [r * rows_per, ...) of the
 // row block: every CTA pushes its partials of those rows into the owner's
 // shared memory with st.async, which counts the bytes on the owner's
 // mbarrier; the owner adds the cluster's partials in rank order and writes
@@ -274,18 +275,28 @@ __global__ void __launch_bounds__(256) gemv_reduce_kernel(const float* __restric
 // ---------------------------------------------------------------------------
 constexpr int kRingRows = 128;             // weight rows per CTA (one scale-atom row block)
 constexpr int kRingTiles = kRingRows / 16;  // 16-row MMA tiles per CTA
-template <bool kTok16> struct RingShape {
-  static constexpr int kGroups = 2;                         // k-groups
+// Two layouts.  Below kRingWideFromT tokens: two k-groups (16 compute warps),
+// two CTAs per SM, so that the next call's CTAs are resident beside this
+// call's and copy their weights while it computes.  From kRingWideFromT
+// tokens the k-loop has more work per weight byte: three k-groups (24 compute
+// warps, up to 80 registers) and one CTA per SM, whose ring then usually holds
+// the CTA's whole weight slice.
+template <bool kTok16, int kG> struct RingShape {
+  static constexpr int kGroups = kG;                        // k-groups
   static constexpr int kCompWarps = kRingTiles * kGroups;   // one tile per warp
   static constexpr int kThreads = (kCompWarps + 1) * 32;    // + one producer warp
-  static constexpr int kMinBlocks = 2;
+  static constexpr int kMinBlocks = kG == 2 ? 2 : 1;
 };
+constexpr int kRingWideFromT = 4;
+__host__ __device__ constexpr int ring_groups(int64_t T) { return T >= kRingWideFromT ? 3 : 2; }
 constexpr int kRingMaxSlots = 24;
 constexpr int kRingChunk = kRingRows * 64;            // codes of one 128-k block
 constexpr int kRingChunkSf = 1024;                    // its two scale atoms
 constexpr int kRingSlot = kRingChunk + kRingChunkSf;
 constexpr int kRingMaxCluster = 8;
-constexpr size_t kRingSmemBudget = 109 * 1024;        // two CTAs per SM with their static shared memory
+// dynamic shared memory per CTA: two CTAs per SM with their static shared
+// memory, or one
+constexpr size_t ring_smem_budget(int groups) { return groups == 2 ? 109 * 1024 : 220 * 1024; }
 constexpr int kStageLoads = 4;                        // activation units in flight per lane while staging
 
 __device__ __forceinline__ uint32_t mapa_u32(uint32_t local, uint32_t rank) {
@@ -304,8 +315,8 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 
-template <bool kTok16>
-__global__ void __launch_bounds__(RingShape<kTok16>::kThreads, RingShape<kTok16>::kMinBlocks) gemv_ring_kernel(
+template <bool kTok16, int kG>
+__global__ void __launch_bounds__(RingShape<kTok16, kG>::kThreads, RingShape<kTok16, kG>::kMinBlocks) gemv_ring_kernel(
     const __grid_constant__ CUtensorMap cmap, const uint16_t* __restrict__ x, int T, int64_t ldx,
     const uint8_t* __restrict__ w_sf, int N, int K, int kc, int R, const float* __restrict__ d_alpha,
     uint16_t* __restrict__ out, int64_t ldo, int* status) {
@@ -316,8 +327,8 @@ __global__ void __launch_bounds__(RingShape<kTok16>::kThreads, RingShape<kTok16>
   __shared__ __align__(8) uint64_t red_bar;
   __shared__ volatile int abort_flag;
 
-  constexpr int kGroups = RingShape<kTok16>::kGroups;
-  constexpr int kCompWarps = RingShape<kTok16>::kCompWarps;
+  constexpr int kGroups = RingShape<kTok16, kG>::kGroups;
+  constexpr int kCompWarps = RingShape<kTok16, kG>::kCompWarps;
   constexpr int kComp = kCompWarps * 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool producer = (warp == kCompWarps) && lane == 0;
@@ -524,7 +535,7 @@ __global__ void __launch_bounds__(RingShape<kTok16>::kThreads, RingShape<kTok16>
         acc[h][3] = fmaf(blk[h][3], mu.y, acc[h][3]);
       }
     }
-    // the two k-groups' partials, added in a fixed order (group 0 + group 1)
+    // the k-groups' partials, added in a fixed order: group 0 + (group 1 + (...))
     for (int grp = kGroups - 1; grp >= 0; --grp) {
       if (kp == grp) {
 #pragma unroll
@@ -609,15 +620,17 @@ GemvRingPlan gemv_ring_plan(int64_t T, int64_t N, int64_t K, int num_sms) {
     // activations, inverse rescales, partials and the receive buffer
     const size_t fixed = static_cast<size_t>(T) * (kcb * 256 + 16) + static_cast<size_t>(kcb * 16 * 4) +
                          static_cast<size_t>(T * kRingRows * 4) + static_cast<size_t>(ncl * T * rows_per * 4);
-    int64_t slots = fixed < kRingSmemBudget ? static_cast<int64_t>((kRingSmemBudget - fixed) / kRingSlot) : 0;
+    const int64_t groups = ring_groups(T);
+    const size_t budget = ring_smem_budget(static_cast<int>(groups));
+    int64_t slots = fixed < budget ? static_cast<int64_t>((budget - fixed) / kRingSlot) : 0;
     if (slots > kcb) slots = kcb;
     if (slots > kRingMaxSlots) slots = kRingMaxSlots;
-    // a ring that is refilled is even: each slot then stays with one k-group
-    // (kb and kb + R have the same parity), so no warp waits on a slot two
-    // phases ahead of the last one it read, where the mbarrier parity test
-    // would pass on a stale phase
-    if (slots < kcb && slots > 1) slots &= ~int64_t{1};
-    const bool ok = slots >= 2 || (slots >= 1 && kcb == 1);
+    // a ring that is refilled holds a multiple of the k-groups: each slot then
+    // stays with one k-group (kb and kb + R are dealt to the same group), so
+    // no warp waits on a slot two phases ahead of the last one it read, where
+    // the mbarrier parity test would pass on a stale phase
+    if (slots < kcb && slots > 1) slots -= slots % groups;
+    const bool ok = slots >= groups || (slots >= 1 && slots >= kcb);
     const bool roomy = slots >= kcb || slots >= 4;
     if ((ok && roomy) || cl >= kRingMaxCluster || cl >= kblocks) {
       p.cl = static_cast<int>(ncl);
@@ -631,16 +644,16 @@ GemvRingPlan gemv_ring_plan(int64_t T, int64_t N, int64_t K, int num_sms) {
   }
 }
 
-template <bool kTok16>
+template <bool kTok16, int kG>
 static cudaError_t launch_ring_t(const CUtensorMap& cmap, const void* x, int64_t T, int64_t ldx, const uint8_t* w_sf,
                                  int64_t N, int64_t K, const float* d_alpha, void* out, int64_t ldo,
                                  const GemvRingPlan& plan, int* status, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(gemv_ring_kernel<kTok16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kRingSmemBudget + 1024));
+  cudaError_t e = cudaFuncSetAttribute(gemv_ring_kernel<kTok16, kG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(ring_smem_budget(kG) + 1024));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(plan.row_blocks * plan.cl));
-  cfg.blockDim = dim3(RingShape<kTok16>::kThreads);
+  cfg.blockDim = dim3(RingShape<kTok16, kG>::kThreads);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -652,7 +665,7 @@ static cudaError_t launch_ring_t(const CUtensorMap& cmap, const void* x, int64_t
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemv_ring_kernel<kTok16>, cmap, static_cast<const uint16_t*>(x),
+  return cudaLaunchKernelEx(&cfg, gemv_ring_kernel<kTok16, kG>, cmap, static_cast<const uint16_t*>(x),
                             static_cast<int>(T), ldx, w_sf, static_cast<int>(N), static_cast<int>(K), plan.kc, plan.R,
                             d_alpha, static_cast<uint16_t*>(out), ldo, status);
 }
@@ -660,8 +673,11 @@ static cudaError_t launch_ring_t(const CUtensorMap& cmap, const void* x, int64_t
 cudaError_t launch_gemv_w4a16_ring(const CUtensorMap& cmap, const void* x, int64_t T, int64_t ldx,
                                    const uint8_t* w_sf, int64_t N, int64_t K, const float* d_alpha, void* out,
                                    int64_t ldo, const GemvRingPlan& plan, int* status, cudaStream_t stream) {
-  if (T > 8) return launch_ring_t<true>(cmap, x, T, ldx, w_sf, N, K, d_alpha, out, ldo, plan, status, stream);
-  return launch_ring_t<false>(cmap, x, T, ldx, w_sf, N, K, d_alpha, out, ldo, plan, status, stream);
+  static_assert(kRingWideFromT <= 8, "T > 8 runs the three-group layout");
+  if (T > 8) return launch_ring_t<true, 3>(cmap, x, T, ldx, w_sf, N, K, d_alpha, out, ldo, plan, status, stream);
+  if (ring_groups(T) == 3)
+    return launch_ring_t<false, 3>(cmap, x, T, ldx, w_sf, N, K, d_alpha, out, ldo, plan, status, stream);
+  return launch_ring_t<false, 2>(cmap, x, T, ldx, w_sf, N, K, d_alpha, out, ldo, plan, status, stream);
 }
 
 GemvPlan gemv_plan(int64_t T, int64_t N, int64_t K, int num_sms) {
