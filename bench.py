@@ -296,6 +296,26 @@ class Workload:
                 3 * len(self.moe16_banks) * len(self.moe16))
 
 
+def _decode_kernel(T: int) -> str:
+    """The decode GEMM instantiation a call with T tokens runs on these shapes:
+    two k-groups below 4 tokens, three from 4; 16 tokens per MMA pass above 8."""
+    return f"gemv_ring_kernel<{1 if T > 8 else 0}, {3 if T >= 4 else 2}>"
+
+
+def _decode_kernel_rooflines(wl, decode: dict, hbm: float) -> dict:
+    """Per decode instantiation: its share of the step's decode time (every
+    graph replays its calls once per step) and its time-weighted bandwidth."""
+    agg = {}
+    for d in wl.decode:
+        t = decode[f"T{d['T']}_{d['N']}x{d['K']}"]["us"] * 1e-6
+        a = agg.setdefault(_decode_kernel(d["T"]), [0.0, 0.0])
+        a[0] += d["ncopy"] * t
+        a[1] += d["ncopy"] * d["bytes"]
+    total = sum(v[0] for v in agg.values())
+    return {k: {"share_of_decode_time": round(v[0] / total, 4), "gbs": round(v[1] / v[0] / 1e9, 1),
+                "frac_hbm": round(v[1] / v[0] / 1e9 / hbm, 4)} for k, v in agg.items()}
+
+
 def _profile_traffic(name: str):
     """DRAM bytes per launch recorded in profiles/<name> by an ncu capture, or
     None when the kernel source has changed since (its git blob hash differs
@@ -620,7 +640,9 @@ def run_ours(args, world, rank, local):
         "configs": configs,
         # the dominant kernel of the step (most of its device time, by the ncu
         # launch list of this command) is the decode GEMM; its roofline is
-        # given for the headline decode call, T = 1 on 8704 x 5120
+        # given for the headline decode call, T = 1 on 8704 x 5120, and per
+        # instantiation below
+        "roofline_decode_kernels": _decode_kernel_rooflines(wl, decode, hbm),
         "roofline": {"kernel": "gemv_ring_kernel<0, 2> (W4A16 decode, T=1, 8704x5120)", "bound": "hbm",
                      "achieved": round(head["gbs"], 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(head["gbs"] / hbm, 4),
