@@ -382,12 +382,14 @@ def test_fused_parts_use_largest_global():
 # MoE
 # ---------------------------------------------------------------------------
 
-def test_moe_align_matches_numpy():
-    rng = np.random.default_rng(4)
-    T, topk, E, BM = 50, 4, 9, 16
+@pytest.mark.parametrize("T,topk,E,BM", [(50, 4, 9, 16), (300, 8, 5, 128), (700, 4, 3, 256), (90, 2, 64, 256)])
+def test_moe_align_matches_numpy(T, topk, E, BM):
+    """The stable counting sort with BM-row segments (the 128- and 256-row
+    paddings the GEMM tiles use among them) against numpy's stable argsort."""
+    rng = np.random.default_rng(4 + BM)
     ids = rng.integers(0, E, size=(T, topk)).astype(np.int32)
     ids[3, 1] = -1
-    ids[7, 2] = E  # invalid ids are dropped
+    ids[7, topk - 1] = E  # invalid ids are dropped
     res = oracle.moe_align(torch.from_numpy(ids), E, BM)
     flat = ids.ravel()
     valid = (flat >= 0) & (flat < E)
