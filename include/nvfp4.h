@@ -139,7 +139,8 @@ size_t nvfp4_linear_w4a16_workspace(int64_t T, int64_t N, int64_t K);
  *   that is 0).  The k-split partial sums of a 128-row block are summed on
  *   chip, inside a thread-block cluster, so the query returns 0, unless the
  *   activations of one k-split do not fit in shared memory next to the weight
- *   (long K at large T, e.g. T = 16 with K > 24576); those shapes keep fp32
+ *   (long K at large T: on 152 SMs from K = 44160 at T = 16 and from
+ *   K = 91264 at T = 8, whatever N); those shapes keep fp32
  *   partials in the workspace and sum them with a second kernel.  Either way
  *   the partials are summed in a fixed order, so the result is the same from
  *   run to run.

@@ -75,6 +75,22 @@ def test_quant_and_w4a16_argument_errors(lib):
     assert na(P, 17, 512, P, P, 64, 512, P, P, 64, None) == 2                # T > 16
 
 
+def test_w4a16_workspace_only_for_long_k_at_large_t(lib):
+    """The decode sums its k-split partials on chip unless the activations of
+    one k-split leave too little shared memory for the weight ring; the
+    boundary (host planning, 152 SMs when no device is present) does not
+    depend on N."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("the boundary is stated for 152 SMs")
+    q = lib.nvfp4_linear_w4a16_workspace
+    for N in (1024, 8704):
+        assert q(1, N, 131072) == 0 and q(4, N, 131072) == 0
+        assert q(8, N, 91136) == 0 and q(8, N, 91264) > 0
+        assert q(16, N, 44032) == 0 and q(16, N, 44160) > 0
+        assert q(16, N, 5120) == 0 and q(16, N, 4352) == 0     # the decode workloads
+
+
 def test_no_device_is_reported_without_a_gpu(lib):
     import torch
     if torch.cuda.is_available():
