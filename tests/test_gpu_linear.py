@@ -140,14 +140,18 @@ def test_w4a16_decode_shapes(nv, T, N, K):
 
 @pytest.mark.parametrize("T,N,K", [(1, 8, 128), (3, 136, 384), (5, 1032, 256), (7, 264, 640),
                                    (9, 520, 128), (15, 2056, 1152), (16, 16, 4096), (2, 3584, 5120),
-                                   (1, 256, 32768), (16, 128, 16384), (16, 256, 32768)])
+                                   (1, 256, 32768), (16, 128, 16384), (16, 128, 44032),
+                                   (16, 256, 45056), (8, 136, 91264)])
 def test_w4a16_ragged(nv, T, N, K):
     """Ragged N (partial 128-row blocks), T across both token layouts, and long
     K: (1, 256, 32768) and (16, 128, 16384) stream more 128-k blocks than the
-    shared-memory ring holds (the latter through a ring of two slots that
-    alternate between the two k-groups' warps), (16, 256, 32768) has more
-    activations per CTA than fit next to the ring and runs the split-K kernel
-    with its workspace."""
+    shared-memory ring holds; (16, 128, 44032) is the longest K at T = 16 whose
+    k-split activations still fit beside the ring, so its partials are summed
+    on chip; (16, 256, 45056) and (8, 136, 91264) are past that boundary and run
+    the split-K kernel with its workspace."""
+    need = nv.nvfp4_linear_w4a16_workspace(T, N, K)
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert (need > 0) == (K > 44032 if T > 8 else K > 91136), (T, N, K, need)
     L = Linear(nv, synthdata.decode_case(T, N, K, seed=N + T), quant_act=False)
     out = nv.nvfp4_linear_w4a16(L.x_dev, L.W.codes, L.W.scales, L.alpha16_dev, N, K)
     check_close(out, oracle.linear_w4a16(L.x, L.wc, L.ws, N, K, L.alpha16), f"W4A16 {T}x{N}x{K}")
