@@ -494,11 +494,18 @@ __global__ void __launch_bounds__(RingShape<kTok16, kG>::kThreads, RingShape<kTo
         s -= R;
         ph ^= 1u;
       }
-      float blk[kH][4];
+      // in the two-group layout the two MMAs of a code word go to separate
+      // accumulators (two chains of four dependent MMAs per block instead of
+      // one of eight: 1-2 % per call at 1-2 tokens); the three-group layouts
+      // keep one chain, where the extra registers bought nothing
+      constexpr int kS = (kTok16 || kG == 3) ? 1 : 2;
+      float blk[kH][4], blk2[kS == 2 ? kH : 1][4];
 #pragma unroll
       for (int h = 0; h < kH; ++h)
 #pragma unroll
         for (int c = 0; c < 4; ++c) blk[h][c] = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) blk2[0][c] = 0.0f;
       const uint8_t* xb = xs + kb * 256;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -517,7 +524,7 @@ __global__ void __launch_bounds__(RingShape<kTok16, kG>::kThreads, RingShape<kTo
         if (tok_lo) xl = *reinterpret_cast<const uint4*>(xb + xofs[i]);
         // A: rows r0 / r1, k pairs (0,1) then (2,3) of code word i
         mma_f16_16816(blk[0], a[0], b[0], a[1], b[1], xl.x, xl.y);
-        mma_f16_16816(blk[0], a[2], b[2], a[3], b[3], xl.z, xl.w);
+        mma_f16_16816(kS == 2 ? blk2[0] : blk[0], a[2], b[2], a[3], b[3], xl.z, xl.w);
         if constexpr (kTok16) {
           uint4 xh = make_uint4(0u, 0u, 0u, 0u);
           if (tok_hi) xh = *reinterpret_cast<const uint4*>(xb + xofs[i] + 8 * xs_stride);
@@ -529,6 +536,10 @@ __global__ void __launch_bounds__(RingShape<kTok16, kG>::kThreads, RingShape<kTo
 #pragma unroll
       for (int h = 0; h < kH; ++h) {
         const float2 mu = *reinterpret_cast<const float2*>(xmul + kb * 16 + 8 * h + 2 * t);
+        if constexpr (kS == 2) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) blk[h][c] += blk2[h][c];
+        }
         acc[h][0] = fmaf(blk[h][0], mu.x, acc[h][0]);
         acc[h][1] = fmaf(blk[h][1], mu.y, acc[h][1]);
         acc[h][2] = fmaf(blk[h][2], mu.x, acc[h][2]);
