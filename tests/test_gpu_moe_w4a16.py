@@ -125,6 +125,33 @@ def test_moe_w4a16_duplicate_and_invalid_ids(nv, small):
     check_close(out.cpu(), small.ref(c.x, ids, c.topk_w), "W4A16 MoE duplicate / invalid ids")
 
 
+def test_moe_w4a16_unrouted_token_and_dirty_workspace(nv, small):
+    """A token whose ids are all invalid gets a zero row; the workspace needs
+    no initialisation, so calls that reuse one workspace filled with 0xFF
+    agree bit for bit; and every output element is written (out starts as
+    NaN)."""
+    c = synthdata.moe_case(6, S["E"], S["H"], S["I"], S["topk"], S["skewed"], seed=14, device="cpu")
+    ids = c.topk_ids.clone()
+    ids[4, :] = -1            # no valid route
+    ids[5, 2:] = S["E"]       # two valid routes of eight
+    T, topk = ids.shape
+    ws = torch.full((nv.nvfp4_moe_w4a16_workspace(T, S["H"], S["I"], S["E"], topk),), 0xFF, dtype=torch.uint8,
+                    device=DEV)
+    outs = []
+    for i in range(3):
+        out = torch.full((T, S["H"]), float("nan"), dtype=torch.bfloat16, device=DEV)
+        nv.nvfp4_moe_w4a16(c.x.to(DEV), ids.to(DEV), c.topk_w.to(DEV), small.W.w13_codes, small.W.w13_sf,
+                           small.a13_dev, small.W.w2_codes, small.W.w2_sf, small.a2_dev, S["E"], S["I"], out=out,
+                           workspace=ws)
+        assert nv.nvfp4_device_status() == 7  # NVFP4_ERR_BAD_EXPERT_ID, raised by every call
+        outs.append(out)
+    assert not torch.isnan(outs[0]).any()
+    assert torch.count_nonzero(outs[0][4]).item() == 0
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0]), "W4A16 MoE calls on a reused workspace differ"
+    check_close(outs[0].cpu(), small.ref(c.x, ids, c.topk_w), "W4A16 MoE unrouted token")
+
+
 def test_moe_w4a16_one_expert_for_all_routes(nv, small):
     """160 routes on one expert: more than one pass of 16 input rows."""
     c = synthdata.moe_case(20, S["E"], S["H"], S["I"], S["topk"], S["skewed"], seed=12, device="cpu")
