@@ -267,6 +267,9 @@ nvfp4_status nvfp4_moe_w4a16(const void* x_bf16, int64_t T, int64_t H, int64_t I
  *   n_tiles     int32 [1]         P / 128
  *   row_map     int32 [P_max]     t * topk + slot of each permuted row, -1 for padding
  *   tile_expert int32 [P_max/128] expert of each 128-row tile
+ *   pos         int32 [T*topk]    permuted row of each route, -1 if dropped
+ *   hist        int32 [chunks, E] routes per expert in each chunk of routes
+ *                                 (align's working space above 4096 routes)
  *   a1_codes    u8 [P_max, H/2]   quantised x at the permuted rows
  *   a1_sf       swizzled over P_max rows
  *   h_codes     u8 [P_max, I/2]   quantised SiLU(gate) * up

@@ -122,6 +122,30 @@ def test_moe_workspace_layout(lib):
     assert f(*args) == 2   # H % 128
 
 
+@pytest.mark.parametrize("T,H,I,E,topk", [
+    (1, 128, 128, 1, 1), (16, 2048, 768, 128, 8), (4096, 2048, 768, 128, 8), (16384, 2048, 768, 128, 8),
+    (32768, 7168, 2048, 256, 8), (175001, 256, 128, 3, 3), (3001, 128, 256, 1024, 3), (8, 7168, 2048, 256, 256)])
+def test_moe_layout_regions_are_aligned_disjoint_and_large_enough(lib, T, H, I, E, topk):
+    """Every region of the workspace layout starts on a 256-byte boundary,
+    holds at least what the header says it holds, overlaps no other region
+    and ends inside the total the workspace query reports (the last case is
+    the calibration layout, every row routed to every expert)."""
+    lay = nv.nvfp4_moe_workspace_layout(T, H, I, E, topk)
+    R = T * topk
+    bm = 256 if R >= 1024 * E and H % 256 == 0 else 128
+    assert lay.row_block == bm
+    P = lay.p_max
+    assert P == -(-(R + E * (bm - 1)) // bm) * bm and P % 128 == 0
+    need = {"counts": 4 * E, "offsets": 4 * (E + 1), "n_tiles": 4, "row_map": 4 * P, "tile_expert": 4 * (P // 128),
+            "pos": 4 * R, "hist": 4 * E, "a1_codes": P * H // 2, "a1_sf": oracle.scale_bytes(P, H),
+            "h_codes": P * I // 2, "h_sf": oracle.scale_bytes(P, I), "y": 4 * T * H}
+    regions = sorted((getattr(lay, n), n) for n in need)
+    for (off, n), nxt in zip(regions, regions[1:] + [(lay.total, "total")]):
+        assert off % 256 == 0, n
+        assert off + need[n] <= nxt[0], f"{n} overlaps {nxt[1]}"
+    assert lay.total == lib.nvfp4_moe_workspace(T, H, I, E, topk)
+
+
 def test_moe_w4a16_argument_errors(lib):
     ws = lib.nvfp4_moe_w4a16_workspace
     R = 4 * 8
