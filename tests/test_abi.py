@@ -75,6 +75,58 @@ def test_quant_and_w4a16_argument_errors(lib):
     assert na(P, 17, 512, P, P, 64, 512, P, P, 64, None) == 2                # T > 16
 
 
+def test_helper_and_layer_argument_errors(lib):
+    """The documented status of every argument error that is refused before a
+    device is looked for (1 invalid argument, 2 unsupported shape, 3
+    misaligned, 4 workspace too small; 0 for nothing to do)."""
+    Q = ctypes.c_void_p(264)        # 8-byte aligned only
+    big, small = ctypes.c_size_t(1 << 40), ctypes.c_size_t(16)
+    g = lib.nvfp4_compute_global
+    assert g(None, 4, 64, 64, P, None) == 1                       # null x
+    assert g(P, 4, 64, 32, P, None) == 1                          # ldx < cols
+    assert g(Q, 4, 64, 64, P, None) == 3                          # x not 16-byte aligned
+    assert g(P, 4, 64, 68, P, None) == 3                          # ldx % 8
+    a = lib.nvfp4_make_alpha
+    assert a(P, None, 4, P, None) == 1 and a(P, P, -1, P, None) == 1
+    assert a(None, P, 0, P, None) == 0                            # n = 0: nothing to do
+    r = lib.nvfp4_reduce_max
+    assert r(P, 0, P, None) == 1 and r(None, 4, P, None) == 1
+    w = lib.nvfp4_linear_w4a16
+    assert w(P, 4, 256, P, P, 64, 512, P, P, 64, None, 0, None) == 1     # ldx < K
+    assert w(P, 4, 512, P, P, 64, 512, P, P, 32, None, 0, None) == 1     # ldo < N
+    assert w(P, 4, 512, P, P, 60, 512, P, P, 64, None, 0, None) == 2     # N % 8
+    assert w(Q, 4, 512, P, P, 64, 512, P, P, 64, None, 0, None) == 3     # x misaligned
+    assert w(P, 4, 512, P, P, 64, 512, P, P, 65, None, 0, None) == 3     # odd ldo
+    assert w(P, 4, 512, P, P, 64, 512, P, ctypes.c_void_p(258), 64, None, 0, None) == 3   # out not 4-byte aligned
+    assert w(P, 4, 512, None, P, 64, 512, P, P, 64, None, 0, None) == 1  # null codes
+    l4 = lib.nvfp4_linear_w4a4
+    assert l4(P, Q, 8, P, P, 16, 512, P, P, 16, None) == 3              # scales misaligned
+    m = lib.nvfp4_moe_w4a4
+    args = [P, 16, 2048, 768, 128, 8] + [P] * 12 + [big, None]
+    import torch
+    if not torch.cuda.is_available():
+        assert m(*args) == 8                                     # valid arguments, no device
+    args[4] = 1025
+    assert m(*args) == 2                                         # E > 1024
+    args[4] = 128
+    args[6] = ctypes.c_void_p(258)
+    assert m(*args) == 3                                         # ids not 4-byte aligned
+    args[6] = P
+    args[-2] = small
+    assert m(*args) == 4                                         # workspace too small
+    args[-2] = big
+    args[16] = None
+    assert m(*args) == 1                                         # null out
+    c = lib.nvfp4_moe_calibrate
+    cargs = [P, 16, 2048, 768, 128, P, P, P, P, None, P, P, big, None]
+    assert c(*cargs[:1], 0, *cargs[2:]) == 1                     # no calibration rows
+    assert c(*cargs[:4], 1025, *cargs[5:]) == 2                  # E > 1024
+    assert c(Q, *cargs[1:]) == 3                                 # x misaligned
+    assert c(*cargs[:12], small, None) == 4                      # workspace too small
+    assert c(*cargs[:10], None, *cargs[11:]) == 1                # null g_a2 (amax is optional)
+    assert lib.nvfp4_device_status(None, None) == 1
+
+
 def test_w4a16_workspace_only_for_long_k_at_large_t(lib):
     """The decode sums its k-split partials on chip unless the activations of
     one k-split leave too little shared memory for the weight ring; the
